@@ -1,10 +1,13 @@
 """GB300-native ring-ordered blockwise exact attention.
 
-The compute path is the C-ABI library ``libra.so`` built from ``csrc/``; this
-package only marshals arguments to it (see ``binding``).  Importing the package
-does not load the library; the first compute call does, and raises if the
-library has not been built.
+The compute path is the C-ABI library ``libra.so`` built from ``csrc/`` (see
+``include/ra.h``); ``binding`` only marshals arguments to it.  Importing the
+package does not load the library; the first compute call does, and raises if
+the library has not been built (``build.build()``).
 """
 from . import inputs  # noqa: F401
+from .binding import (RaError, check, forward, lib, merge, permute,  # noqa: F401
+                      schedule_stats, status_string, version, workspace_bytes)
 
-__all__ = ["inputs"]
+__all__ = ["inputs", "RaError", "check", "forward", "lib", "merge", "permute",
+           "schedule_stats", "status_string", "version", "workspace_bytes"]

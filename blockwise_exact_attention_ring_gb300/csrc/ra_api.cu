@@ -1,0 +1,473 @@
+// C-ABI layer of libra.so: argument validation, workspace layout, the host
+// ring-step scheduler, and the stream-ordered launch sequence.  See
+// include/ra.h for the contract of every entry point.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "../../include/ra.h"
+#include "ra_internal.h"
+#include "ra_schedule.h"
+
+namespace {
+
+
+
+constexpr unsigned long long kDefaultTimeoutNs = 4000000000ull;  // 4 s per wait
+unsigned long long g_timeout_ns = kDefaultTimeoutNs;
+std::atomic<unsigned long long> g_launches{0};
+
+void count_launch(unsigned long long n = 1) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int sm_count_current()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        return 1;
+    return n;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb)
+{
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Problem {
+    int B, H, Hkv, S, d, N, layout, causal, dtype, mode;
+    bool rank_major = false;  // inputs/outputs already in the layout's rank order
+    long long L() const { return S / N; }
+    size_t esz() const { return dtype == RA_DTYPE_F32 ? 4 : 2; }
+    size_t q_elems() const { return (size_t)B * H * S * d; }
+    size_t kv_elems() const { return (size_t)B * Hkv * S * d; }
+    size_t rows() const { return (size_t)B * H * S; }
+};
+
+// Validation shared by every forward entry point.  Returns RA_OK or the
+// status to report.
+ra_status check_problem(const Problem &p)
+{
+    if (p.B < 1 || p.H < 1 || p.Hkv < 1 || p.S < 1 || p.d < 1 || p.N < 1)
+        return RA_ERR_INVALID_ARG;
+    if (p.H % p.Hkv != 0 || p.S % p.N != 0)
+        return RA_ERR_INVALID_ARG;
+    if (p.layout != RA_LAYOUT_CONTIGUOUS && p.layout != RA_LAYOUT_STRIPED)
+        return RA_ERR_INVALID_ARG;
+    if (p.causal != 0 && p.causal != 1)
+        return RA_ERR_INVALID_ARG;
+    if (p.dtype != RA_DTYPE_BF16 && p.dtype != RA_DTYPE_F32)
+        return RA_ERR_INVALID_ARG;
+    if (p.mode != RA_MODE_FUSED && p.mode != RA_MODE_PER_STEP)
+        return RA_ERR_INVALID_ARG;
+    // 32-bit TMA row coordinates and grid limits
+    if ((long long)p.B * p.H * p.S >= (1ll << 31) || (long long)p.B * p.H > 65535)
+        return RA_ERR_UNSUPPORTED;
+    if (p.dtype == RA_DTYPE_BF16 && p.d != 64 && p.d != 128)
+        return RA_ERR_UNSUPPORTED;
+    if (p.dtype == RA_DTYPE_F32 && p.d > 256)
+        return RA_ERR_UNSUPPORTED;
+    if (p.mode == RA_MODE_PER_STEP && p.d % 4 != 0)
+        return RA_ERR_UNSUPPORTED;
+    return RA_OK;
+}
+
+// Workspace layout (each region 256-byte aligned):
+//   striped:            q', k', v' in striped order
+//   striped and fused:  out', lse' in striped order
+//   per-step:           running out/lse (fp32) and step partial out/lse (fp32)
+struct WsLayout {
+    size_t q = 0, k = 0, v = 0, out = 0, lse = 0, run = 0, run_lse = 0, part = 0, part_lse = 0;
+    size_t total = 0;
+};
+
+WsLayout ws_layout(const Problem &p)
+{
+    WsLayout w;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += align256(bytes);
+        return at;
+    };
+    if (p.layout == RA_LAYOUT_STRIPED && !p.rank_major) {
+        w.q = take(p.q_elems() * p.esz());
+        w.k = take(p.kv_elems() * p.esz());
+        w.v = take(p.kv_elems() * p.esz());
+        if (p.mode == RA_MODE_FUSED) {
+            w.out = take(p.q_elems() * p.esz());
+            w.lse = take(p.rows() * 4);
+        }
+    }
+    if (p.mode == RA_MODE_PER_STEP) {
+        w.run = take(p.q_elems() * 4);
+        w.run_lse = take(p.rows() * 4);
+        w.part = take(p.q_elems() * 4);
+        w.part_lse = take(p.rows() * 4);
+    }
+    w.total = off;
+    return w;
+}
+
+// ------------------------------------------------------------------ scheduler
+// Units for the tensor-core kernel: pairs of 128-row query tiles sharing a kv
+// head, cost = key tiles visited over ring steps [s_begin, s_end), sorted
+// heaviest first (stable), units that visit nothing dropped.
+std::vector<RaUnit> build_units(int B, int H, int Hkv, int S, int N, int layout, int causal,
+                                int s_begin, int s_end)
+{
+    const int L = S / N;
+    const int ntiles = (L + RA_TILE - 1) / RA_TILE;
+    const int group = H / Hkv;
+    std::vector<RaUnit> units;
+    auto cost_of = [&](int i, int ta_max) {
+        int c = 0;
+        for (int s = s_begin; s < s_end; ++s)
+            c += ra_kv_tiles(ra_block_class(layout, causal, i, ra_ring_block(i, s, N)), ta_max, ntiles);
+        return c;
+    };
+    auto push = [&](int bh0, int ta0, int bh1, int ta1, int i, bool valid1) {
+        RaUnit u{};
+        u.bh0 = bh0, u.ta0 = ta0, u.bh1 = bh1, u.ta1 = ta1, u.rank = i;
+        u.tile1_valid = valid1 ? 1 : 0;
+        u.cost = cost_of(i, std::max(ta0, ta1));
+        if (u.cost > 0)
+            units.push_back(u);
+    };
+    if (group % 2 == 0) {
+        // two query heads of one kv group, same positions: identical masks
+        for (int b = 0; b < B; ++b)
+            for (int h = 0; h < H; h += 2)
+                for (int i = 0; i < N; ++i)
+                    for (int ta = 0; ta < ntiles; ++ta)
+                        push(b * H + h, ta, b * H + h + 1, ta, i, true);
+    } else {
+        // two adjacent query tiles of one head
+        for (int b = 0; b < B; ++b)
+            for (int h = 0; h < H; ++h)
+                for (int i = 0; i < N; ++i)
+                    for (int ta = 0; ta < ntiles; ta += 2) {
+                        const bool has1 = ta + 1 < ntiles;
+                        push(b * H + h, ta, b * H + h, has1 ? ta + 1 : ta, i, has1);
+                    }
+    }
+    std::stable_sort(units.begin(), units.end(),
+                     [](const RaUnit &x, const RaUnit &y) { return x.cost > y.cost; });
+    return units;
+}
+
+struct DeviceUnits {
+    RaUnit *ptr = nullptr;
+    int count = 0;
+};
+
+std::mutex g_sched_mu;
+std::map<std::tuple<int, int, int, int, int, int, int, int, int, int>, DeviceUnits> g_sched;
+
+// Device copy of the unit list, built once per (device, problem, step range)
+// and kept for the life of the process.
+ra_status get_units(int B, int H, int Hkv, int S, int N, int layout, int causal, int s_begin,
+                    int s_end, DeviceUnits *out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return RA_ERR_CUDA;
+    const auto key = std::make_tuple(dev, B, H, Hkv, S, N, layout, causal, s_begin, s_end);
+    std::lock_guard<std::mutex> lock(g_sched_mu);
+    auto it = g_sched.find(key);
+    if (it != g_sched.end()) {
+        *out = it->second;
+        return RA_OK;
+    }
+    std::vector<RaUnit> units = build_units(B, H, Hkv, S, N, layout, causal, s_begin, s_end);
+    DeviceUnits du;
+    du.count = (int)units.size();
+    if (!units.empty()) {
+        if (cudaMalloc(&du.ptr, units.size() * sizeof(RaUnit)) != cudaSuccess)
+            return RA_ERR_NO_MEMORY;
+        if (cudaMemcpy(du.ptr, units.data(), units.size() * sizeof(RaUnit), cudaMemcpyHostToDevice) !=
+            cudaSuccess) {
+            cudaFree(du.ptr);
+            return RA_ERR_CUDA;
+        }
+    }
+    g_sched[key] = du;
+    *out = du;
+    return RA_OK;
+}
+
+// ------------------------------------------------------------------ forward
+ra_status attention_pass(const Problem &p, const void *q, const void *k, const void *v, void *out,
+                         float *lse, int s_begin, int s_end, bool out_f32, int sm, cudaStream_t st)
+{
+    if (p.dtype == RA_DTYPE_F32) {
+        ra::launch_attn_f32((const float *)q, (const float *)k, (const float *)v, (float *)out, lse,
+                            p.B, p.H, p.Hkv, p.S, p.d, p.N, p.layout, p.causal, s_begin, s_end, st);
+        count_launch();
+        return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+    }
+    DeviceUnits du;
+    ra_status rs = get_units(p.B, p.H, p.Hkv, p.S, p.N, p.layout, p.causal, s_begin, s_end, &du);
+    if (rs != RA_OK)
+        return rs;
+    ra::TcLaunch a{};
+    a.q = q, a.k = k, a.v = v, a.out = out, a.lse = lse;
+    a.units = du.ptr, a.n_units = du.count;
+    a.B = p.B, a.H = p.H, a.Hkv = p.Hkv, a.S = p.S, a.d = p.d, a.N = p.N;
+    a.layout = p.layout, a.causal = p.causal, a.s_begin = s_begin, a.s_end = s_end;
+    a.out_f32 = out_f32 ? 1 : 0;
+    a.timeout_ns = g_timeout_ns;
+    a.sm_count = sm;
+    if (a.n_units > 0)
+        count_launch();
+    return ra::launch_attn_tc(a, st) == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+}
+
+ra_status forward_impl(const Problem &p, const void *q, const void *k, const void *v, void *out,
+                       float *lse, void *ws, size_t ws_bytes, cudaStream_t st)
+{
+    ra_status rs = check_problem(p);
+    if (rs != RA_OK)
+        return rs;
+    if (!q || !k || !v || !out || !lse)
+        return RA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+        return RA_ERR_INVALID_ARG;
+    const size_t qb = p.q_elems() * p.esz(), kvb = p.kv_elems() * p.esz(), lb = p.rows() * 4;
+    for (const void *in : {q, k, v})
+        if (overlaps(out, qb, in, in == q ? qb : kvb) || overlaps(lse, lb, in, in == q ? qb : kvb))
+            return RA_ERR_INVALID_ARG;
+    if (overlaps(out, qb, lse, lb))
+        return RA_ERR_INVALID_ARG;
+    const WsLayout w = ws_layout(p);
+    if (w.total > 0 && (!ws || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u)))
+        return RA_ERR_WORKSPACE;
+
+    const int sm = sm_count_current();
+    char *base = static_cast<char *>(ws);
+    const bool striped = p.layout == RA_LAYOUT_STRIPED && !p.rank_major;
+    const long long row_bytes = (long long)p.d * (long long)p.esz();
+    const void *qk = q, *kk = k, *vk = v;
+    if (striped) {
+        ra::launch_permute(q, base + w.q, (long long)p.B * p.H * p.S, p.S, p.N, row_bytes, 0, sm, st);
+        ra::launch_permute(k, base + w.k, (long long)p.B * p.Hkv * p.S, p.S, p.N, row_bytes, 0, sm, st);
+        ra::launch_permute(v, base + w.v, (long long)p.B * p.Hkv * p.S, p.S, p.N, row_bytes, 0, sm, st);
+        count_launch(3);
+        if (cudaGetLastError() != cudaSuccess)
+            return RA_ERR_CUDA;
+        qk = base + w.q, kk = base + w.k, vk = base + w.v;
+    }
+
+    if (p.mode == RA_MODE_FUSED) {
+        void *ok_out = striped ? (void *)(base + w.out) : out;
+        float *ok_lse = striped ? (float *)(base + w.lse) : lse;
+        rs = attention_pass(p, qk, kk, vk, ok_out, ok_lse, 0, p.N, p.dtype == RA_DTYPE_F32, sm, st);
+        if (rs != RA_OK)
+            return rs;
+        if (striped) {
+            ra::launch_permute(ok_out, out, (long long)p.rows(), p.S, p.N, row_bytes, 1, sm, st);
+            ra::launch_permute(ok_lse, lse, (long long)p.rows(), p.S, p.N, 4, 1, sm, st);
+            count_launch(2);
+            if (cudaGetLastError() != cudaSuccess)
+                return RA_ERR_CUDA;
+        }
+        return RA_OK;
+    }
+
+    // per-step: step 0 initialises the running state, later steps are merged
+    float *run = (float *)(base + w.run), *run_lse = (float *)(base + w.run_lse);
+    float *part = (float *)(base + w.part), *part_lse = (float *)(base + w.part_lse);
+    rs = attention_pass(p, qk, kk, vk, run, run_lse, 0, 1, true, sm, st);
+    if (rs != RA_OK)
+        return rs;
+    const long long L = p.L();
+    for (int s = 1; s < p.N; ++s) {
+        rs = attention_pass(p, qk, kk, vk, part, part_lse, s, s + 1, true, sm, st);
+        if (rs != RA_OK)
+            return rs;
+        // contiguous causal: at step s only ranks i >= s hold a visible block
+        const long long begin = (p.causal && p.layout == RA_LAYOUT_CONTIGUOUS) ? s * L : 0;
+        ra::launch_merge(run, run_lse, part, part_lse, (long long)p.B * p.H, p.S, begin, p.S - begin,
+                         p.d, sm, st);
+        count_launch();
+        if (cudaGetLastError() != cudaSuccess)
+            return RA_ERR_CUDA;
+    }
+    ra::launch_finalize(run, run_lse, out, lse, p.dtype == RA_DTYPE_BF16, (long long)p.rows(), p.S,
+                        p.N, striped ? 1 : 0, p.d, sm, st);
+    count_launch();
+    return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+}
+
+ra_status forward_alloc(const Problem &p, const void *q, const void *k, const void *v, void *out,
+                        float *lse, cudaStream_t st)
+{
+    ra_status rs = check_problem(p);
+    if (rs != RA_OK)
+        return rs;
+    const size_t bytes = ws_layout(p).total;
+    void *ws = nullptr;
+    if (bytes > 0 && cudaMallocAsync(&ws, bytes, st) != cudaSuccess) {
+        cudaGetLastError();
+        return RA_ERR_NO_MEMORY;
+    }
+    rs = forward_impl(p, q, k, v, out, lse, ws, bytes, st);
+    if (ws && cudaFreeAsync(ws, st) != cudaSuccess && rs == RA_OK)
+        rs = RA_ERR_CUDA;
+    return rs;
+}
+
+}  // namespace
+
+extern "C" {
+
+ra_status ra_forward(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
+                     int Hkv, int S, int d, int n_blocks, int layout, int causal, ra_stream_t stream)
+{
+    const Problem p{B, H, Hkv, S, d, n_blocks, layout, causal, RA_DTYPE_BF16, RA_MODE_FUSED};
+    return forward_alloc(p, q, k, v, out, lse, (cudaStream_t)stream);
+}
+
+ra_status ra_forward_f32(const float *q, const float *k, const float *v, float *out, float *lse, int B,
+                         int H, int Hkv, int S, int d, int n_blocks, int layout, int causal,
+                         ra_stream_t stream)
+{
+    const Problem p{B, H, Hkv, S, d, n_blocks, layout, causal, RA_DTYPE_F32, RA_MODE_FUSED};
+    return forward_alloc(p, q, k, v, out, lse, (cudaStream_t)stream);
+}
+
+size_t ra_workspace_bytes(int B, int H, int Hkv, int S, int d, int n_blocks, int layout, int causal,
+                          int mode, int dtype)
+{
+    const Problem p{B, H, Hkv, S, d, n_blocks, layout, causal, dtype, mode};
+    if (check_problem(p) != RA_OK)
+        return 0;
+    return ws_layout(p).total;
+}
+
+ra_status ra_forward_ws(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
+                        int Hkv, int S, int d, int n_blocks, int layout, int causal, int dtype, int mode,
+                        void *ws, size_t ws_bytes, ra_stream_t stream)
+{
+    const Problem p{B, H, Hkv, S, d, n_blocks, layout, causal, dtype, mode};
+    return forward_impl(p, q, k, v, out, lse, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+ra_status ra_forward_rank_major(const void *q, const void *k, const void *v, void *out, float *lse, int B,
+                                int H, int Hkv, int S, int d, int n_blocks, int layout, int causal, int dtype,
+                                int mode, void *ws, size_t ws_bytes, ra_stream_t stream)
+{
+    Problem p{B, H, Hkv, S, d, n_blocks, layout, causal, dtype, mode};
+    p.rank_major = true;
+    return forward_impl(p, q, k, v, out, lse, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+unsigned long long ra_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+ra_status ra_permute(const void *src, void *dst, int B, int Hn, int S, int d, int elem_bytes, int n_blocks,
+                     int inverse, ra_stream_t stream)
+{
+    if (!src || !dst || B < 1 || Hn < 1 || S < 1 || d < 1 || n_blocks < 1 || S % n_blocks != 0)
+        return RA_ERR_INVALID_ARG;
+    if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8)
+        return RA_ERR_INVALID_ARG;
+    if (inverse != 0 && inverse != 1)
+        return RA_ERR_INVALID_ARG;
+    const long long row_bytes = (long long)d * elem_bytes;
+    const size_t total = (size_t)B * Hn * S * row_bytes;
+    if (overlaps(src, total, dst, total))
+        return RA_ERR_INVALID_ARG;
+    const uintptr_t mis = (reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst));
+    // vector width is chosen from the row size; pointers must match it
+    if ((row_bytes % 16 == 0 && (mis & 15u)) || (row_bytes % 4 == 0 && (mis & 3u)))
+        return RA_ERR_INVALID_ARG;
+    ra::launch_permute(src, dst, (long long)B * Hn * S, S, n_blocks, row_bytes, inverse,
+                       sm_count_current(), (cudaStream_t)stream);
+    count_launch();
+    return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+}
+
+ra_status ra_merge(float *out_run, float *lse_run, const float *out_s, const float *lse_s, long long rows,
+                   int d, ra_stream_t stream)
+{
+    if (!out_run || !lse_run || !out_s || !lse_s || rows < 1 || d < 4 || d > 256 || d % 4 != 0)
+        return RA_ERR_INVALID_ARG;
+    if (!aligned16(out_run) || !aligned16(out_s) || ((reinterpret_cast<uintptr_t>(lse_run) |
+                                                      reinterpret_cast<uintptr_t>(lse_s)) & 3u))
+        return RA_ERR_INVALID_ARG;
+    const size_t ob = (size_t)rows * d * 4, lb = (size_t)rows * 4;
+    if (overlaps(out_run, ob, out_s, ob) || overlaps(lse_run, lb, lse_s, lb) ||
+        overlaps(out_run, ob, lse_run, lb) || overlaps(out_run, ob, lse_s, lb) ||
+        overlaps(lse_run, lb, out_s, ob))
+        return RA_ERR_INVALID_ARG;
+    ra::launch_merge(out_run, lse_run, out_s, lse_s, 1, rows, 0, rows, d, sm_count_current(),
+                     (cudaStream_t)stream);
+    count_launch();
+    return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+}
+
+ra_status ra_check(ra_stream_t stream)
+{
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess)
+        return RA_ERR_CUDA;
+    unsigned int st = 0;
+    if (ra::read_and_clear_device_status(&st) != cudaSuccess)
+        return RA_ERR_CUDA;
+    if (st == 0)
+        return RA_OK;
+    return (st & 0xffu) == ra::RA_DEV_TIMEOUT_CODE ? RA_ERR_TIMEOUT : RA_ERR_CUDA;
+}
+
+const char *ra_status_string(int status)
+{
+    switch (status) {
+    case RA_OK: return "RA_OK";
+    case RA_ERR_INVALID_ARG: return "RA_ERR_INVALID_ARG";
+    case RA_ERR_UNSUPPORTED: return "RA_ERR_UNSUPPORTED";
+    case RA_ERR_CUDA: return "RA_ERR_CUDA";
+    case RA_ERR_NO_MEMORY: return "RA_ERR_NO_MEMORY";
+    case RA_ERR_TIMEOUT: return "RA_ERR_TIMEOUT";
+    case RA_ERR_WORKSPACE: return "RA_ERR_WORKSPACE";
+    default: return "RA_ERR_UNKNOWN";
+    }
+}
+
+const char *ra_version(void) { return "ra 0.1.0 sm_103a"; }
+
+long long ra_schedule_stats(int layout, int causal, int n_blocks, int L, long long *pairs, long long *tiles)
+{
+    if (n_blocks < 1 || L < 1 || (layout != 0 && layout != 1) || (causal != 0 && causal != 1))
+        return -1;
+    const int ntiles = (L + RA_TILE - 1) / RA_TILE;
+    long long total = 0;
+    for (int i = 0; i < n_blocks; ++i)
+        for (int s = 0; s < n_blocks; ++s) {
+            const int cls = ra_block_class(layout, causal, i, ra_ring_block(i, s, n_blocks));
+            long long np = 0, nt = 0;
+            for (int a = 0; a < L; ++a)
+                np += ra_key_limit(cls, a, L);
+            for (int ta = 0; ta < ntiles; ++ta)
+                nt += ra_kv_tiles(cls, ta, ntiles);
+            if (pairs)
+                pairs[i * n_blocks + s] = np;
+            if (tiles)
+                tiles[i * n_blocks + s] = nt;
+            total += np;
+        }
+    return total;
+}
+
+}  // extern "C"

@@ -1,0 +1,611 @@
+// Tensor-core ring-ordered blockwise attention for sm_103a (GB300).
+//
+// Method ("Ring Attention" glossary page, ultralytics.com/tr, section "Halka
+// Dikkati Nasil Calisir"): query block i stays in place while key/value
+// blocks arrive in ring order j = (i - s) mod N; each block's scores are
+// exponentiated and folded into a running sum of exponentials and a running
+// score-weighted value sum that are divided at the end, with a running
+// maximum subtracted before exponentiation for stability; causal masking
+// skips key blocks that hold no visible key, and the striped layout changes
+// only which tiles are masked.  The page notes that ring attention uses a
+// flash-attention style blockwise kernel per device; this is that kernel,
+// written for Blackwell:
+//
+//   * one persistent CTA per SM (512 TMEM columns, ~193 KB shared memory);
+//   * a unit of work is a PAIR of 128-row query tiles that share a kv head
+//     (two heads of one grouped-query group, or two adjacent tiles of one
+//     head), so every key/value tile staged in shared memory feeds two tiles;
+//   * warp 0 issues TMA loads (Q once per unit, K and V per 128-key tile, in
+//     128-byte swizzled 64-column slabs), warp 1 issues tcgen05.mma,
+//     warps 4-7 and 8-11 run the online softmax for query tile 0 and 1;
+//   * S = Q K^T goes to TMEM (fp32, 128 lanes x 128 columns per tile); the
+//     softmax warps read a row per thread, write P = exp2(S log2e/sqrt(d) - m)
+//     back over the same columns as packed bf16, and O += P V reads P from
+//     TMEM as the A operand and V from shared memory (MN-major);
+//   * the running max is rescaled lazily: O and l are only corrected when a
+//     row's max grows by more than 2^8, which the final division makes exact;
+//   * every mbarrier wait is bounded; a wait that runs out records an error
+//     word, raises a CTA-wide abort flag, drains in-flight copies and MMAs,
+//     frees TMEM and returns.
+//
+// TMEM columns: S/P tile 0 [0,128), S/P tile 1 [128,256), O tile 0
+// [256,256+d), O tile 1 [384,384+d).
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "ra_internal.h"
+#include "ra_ptx.cuh"
+
+namespace ra {
+
+__device__ unsigned int g_ra_status = 0;
+
+namespace {
+
+constexpr int NUM_THREADS = 384;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr float LAZY_RESCALE_LOG2 = 8.0f;
+constexpr float LN2 = 0.693147180559945309f;
+
+enum Site : unsigned int {
+    SITE_Q_EMPTY = 1, SITE_K_EMPTY, SITE_V_EMPTY, SITE_Q_FULL, SITE_K_FULL, SITE_V_FULL,
+    SITE_P_FULL, SITE_O_FREE, SITE_S_FULL, SITE_O_DONE, SITE_FINAL, SITE_DRAIN
+};
+
+template <int D>
+struct Cfg {
+    static constexpr int KSTAGES = 2;
+    static constexpr int VSTAGES = 2;
+    static constexpr int SLAB = 128 * 64 * 2;  // 128 rows x 64 bf16 (128 B swizzled rows)
+    static constexpr int NSLAB = D / 64;
+    static constexpr int TILE = SLAB * NSLAB;
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + 2 * TILE;
+    static constexpr int OFF_V = OFF_K + KSTAGES * TILE;
+    static constexpr int OFF_CTRL = OFF_V + VSTAGES * TILE;
+    static constexpr int SMEM = OFF_CTRL + 256 + 1024;  // control block + alignment slack
+};
+
+struct Ctrl {
+    uint64_t q_full, q_empty;
+    uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+    uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
+    uint64_t final_bar;
+    uint32_t tmem_base;
+    int abort;
+};
+static_assert(sizeof(Ctrl) <= 256, "control block");
+
+struct TcParams {
+    CUtensorMap tm_q, tm_k, tm_v;
+    const RaUnit *units;
+    void *out;
+    float *lse;
+    int n_units, H, Hkv, S, L, N, layout, causal, s_begin, s_end, out_f32, ntiles;
+    float scale_log2;
+    unsigned long long timeout_ns;
+};
+
+// Walks the key tiles of one unit in ring order: steps s in [s_begin, s_end),
+// block j = (i - s) mod N, tiles tb in [0, ra_kv_tiles(...)).
+struct KvWalk {
+    int i, N, layout, causal, ntiles, ta_max, s_end;
+    int s, j, cls, nt, tb;
+
+    __device__ void start(int rank, int tmax, const TcParams &p)
+    {
+        i = rank, N = p.N, layout = p.layout, causal = p.causal, ntiles = p.ntiles;
+        ta_max = tmax, s_end = p.s_end, s = p.s_begin - 1, j = 0, cls = 0, nt = 0;
+        next_block();
+    }
+    __device__ void next_block()
+    {
+        tb = 0;
+        while (++s < s_end) {
+            j = ra_ring_block(i, s, N);
+            cls = ra_block_class(layout, causal, i, j);
+            nt = ra_kv_tiles(cls, ta_max, ntiles);
+            if (nt > 0)
+                return;
+        }
+    }
+    __device__ bool valid() const { return s < s_end; }
+    __device__ void advance()
+    {
+        if (++tb >= nt)
+            next_block();
+    }
+};
+
+// Units are dealt to CTAs in snake order over the cost-sorted list.
+__device__ __forceinline__ int unit_index(int round, int cta, int G)
+{
+    return round * G + ((round & 1) ? (G - 1 - cta) : cta);
+}
+
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          uint64_t timeout, unsigned int site)
+{
+    const bool ok = mbar_wait(bar, parity, abort, timeout, &g_ra_status, site);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, volatile int *abort,
+                                      uint64_t timeout, unsigned int site)
+{
+    return mbar_wait(bar, parity, abort, timeout, &g_ra_status, site);
+}
+
+// Wait that ignores the abort flag: used to drain work already in flight.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout)
+{
+    int never = 0;
+    mbar_wait(bar, parity, &never, timeout, &g_ra_status, SITE_DRAIN);
+}
+
+template <int D>
+__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap *tm, int row, uint32_t bar,
+                                          uint64_t pol)
+{
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h)
+        tma_load_2d(dst + h * Cfg<D>::SLAB, tm, h * 64, row, bar, pol);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+          "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
+          "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid_constant__ TcParams p)
+{
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(smem);
+    Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + C::OFF_CTRL);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    auto bar = [&](uint64_t &b) { return smem_u32(&b); };
+    const uint32_t sQ = sb + C::OFF_Q, sK = sb + C::OFF_K, sV = sb + C::OFF_V;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(ctrl->q_full), 1);
+        mbar_init(bar(ctrl->q_empty), 1);
+        for (int s = 0; s < C::KSTAGES; ++s) {
+            mbar_init(bar(ctrl->k_full[s]), 1);
+            mbar_init(bar(ctrl->k_empty[s]), 1);
+        }
+        for (int s = 0; s < C::VSTAGES; ++s) {
+            mbar_init(bar(ctrl->v_full[s]), 1);
+            mbar_init(bar(ctrl->v_empty[s]), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(ctrl->s_full[t]), 1);
+            mbar_init(bar(ctrl->p_full[t]), 128);
+            mbar_init(bar(ctrl->o_done[t]), 1);
+            mbar_init(bar(ctrl->o_free[t]), 128);
+        }
+        mbar_init(bar(ctrl->final_bar), 1);
+        ctrl->abort = 0;
+        fence_mbar_init();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&p.tm_q);
+        tma_prefetch_desc(&p.tm_k);
+        tma_prefetch_desc(&p.tm_v);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctrl->tmem_base), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctrl->tmem_base;
+    volatile int *abort = &ctrl->abort;
+    const uint64_t tmo = p.timeout_ns;
+    const int group = p.H / p.Hkv;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol_q = l2_policy_evict_first();
+            const uint64_t pol_kv = l2_policy_evict_last();
+            uint32_t kcnt = 0, vcnt = 0, qcnt = 0;
+            bool ok = true;
+            for (int r = 0; ok; ++r) {
+                const int u = unit_index(r, blockIdx.x, gridDim.x);
+                if (u >= p.n_units)
+                    break;
+                const RaUnit U = p.units[u];
+                if (qcnt > 0 && !(ok = wait1(bar(ctrl->q_empty), (qcnt - 1) & 1, abort, tmo,
+                                                 SITE_Q_EMPTY)))
+                    break;
+                mbar_arrive_expect_tx(bar(ctrl->q_full), 2 * C::TILE);
+                const int qrow0 = U.bh0 * p.S + U.rank * p.L + U.ta0 * RA_TILE;
+                const int qrow1 = U.bh1 * p.S + U.rank * p.L + U.ta1 * RA_TILE;
+                load_tile<D>(sQ, &p.tm_q, qrow0, bar(ctrl->q_full), pol_q);
+                load_tile<D>(sQ + C::TILE, &p.tm_q, qrow1, bar(ctrl->q_full), pol_q);
+                ++qcnt;
+                const int b = U.bh0 / p.H;
+                const int kvbh = b * p.Hkv + (U.bh0 - b * p.H) / group;
+                KvWalk w;
+                w.start(U.rank, max(U.ta0, U.ta1), p);
+                for (; w.valid(); w.advance()) {
+                    const int row = kvbh * p.S + w.j * p.L + w.tb * RA_TILE;
+                    const int ks = kcnt % C::KSTAGES;
+                    if (!(ok = wait1(bar(ctrl->k_empty[ks]), ((kcnt / C::KSTAGES) & 1) ^ 1,
+                                         abort, tmo, SITE_K_EMPTY)))
+                        break;
+                    mbar_arrive_expect_tx(bar(ctrl->k_full[ks]), C::TILE);
+                    load_tile<D>(sK + ks * C::TILE, &p.tm_k, row, bar(ctrl->k_full[ks]), pol_kv);
+                    ++kcnt;
+                    const int vs = vcnt % C::VSTAGES;
+                    if (!(ok = wait1(bar(ctrl->v_empty[vs]), ((vcnt / C::VSTAGES) & 1) ^ 1,
+                                         abort, tmo, SITE_V_EMPTY)))
+                        break;
+                    mbar_arrive_expect_tx(bar(ctrl->v_full[vs]), C::TILE);
+                    load_tile<D>(sV + vs * C::TILE, &p.tm_v, row, bar(ctrl->v_full[vs]), pol_kv);
+                    ++vcnt;
+                }
+            }
+            if (!ok) {
+                // let every issued copy land before shared memory is released
+                for (int s = 0; s < C::KSTAGES; ++s) {
+                    const uint32_t n = kcnt > (uint32_t)s ? (kcnt - s + C::KSTAGES - 1) / C::KSTAGES : 0;
+                    if (n)
+                        wait_drain(bar(ctrl->k_full[s]), (n - 1) & 1, tmo);
+                }
+                for (int s = 0; s < C::VSTAGES; ++s) {
+                    const uint32_t n = vcnt > (uint32_t)s ? (vcnt - s + C::VSTAGES - 1) / C::VSTAGES : 0;
+                    if (n)
+                        wait_drain(bar(ctrl->v_full[s]), (n - 1) & 1, tmo);
+                }
+                if (qcnt)
+                    wait_drain(bar(ctrl->q_full), (qcnt - 1) & 1, tmo);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0);
+            constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, 1);
+            auto issue_s = [&](int t, int ks) {
+                const uint32_t qa = sQ + t * C::TILE, ka = sK + ks * C::TILE;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::SLAB + (kk & 3) * 32;
+                    mma_ss(tmem + t * 128, smem_desc_sw128(qa + off, 16, 1024),
+                           smem_desc_sw128(ka + off, 16, 1024), IDESC_S, kk > 0);
+                }
+            };
+            auto issue_pv = [&](int t, int vs, bool acc) {
+                const uint32_t va = sV + vs * C::TILE;
+#pragma unroll
+                for (int kk = 0; kk < RA_TILE / 16; ++kk)
+                    mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
+                           smem_desc_sw128(va + kk * 2048, C::SLAB, 1024), IDESC_PV,
+                           (acc || kk > 0) ? 1u : 0u);
+            };
+            uint32_t kcnt = 0, vcnt = 0, qcnt = 0, pcnt = 0;
+            bool ok = true;
+            for (int r = 0; ok; ++r) {
+                const int u = unit_index(r, blockIdx.x, gridDim.x);
+                if (u >= p.n_units)
+                    break;
+                const int n = p.units[u].cost;
+                if (!(ok = wait1(bar(ctrl->q_full), qcnt & 1, abort, tmo, SITE_Q_FULL)))
+                    break;
+                int ks = kcnt % C::KSTAGES;
+                if (!(ok = wait1(bar(ctrl->k_full[ks]), (kcnt / C::KSTAGES) & 1, abort, tmo,
+                                     SITE_K_FULL)))
+                    break;
+                tc_fence_after();
+                issue_s(0, ks);
+                mma_commit(bar(ctrl->s_full[0]));
+                issue_s(1, ks);
+                mma_commit(bar(ctrl->s_full[1]));
+                mma_commit(bar(ctrl->k_empty[ks]));
+                ++kcnt;
+                if (n == 1)
+                    mma_commit(bar(ctrl->q_empty));
+                for (int jj = 0; jj < n; ++jj) {
+                    const int vs = vcnt % C::VSTAGES;
+                    const bool more = jj + 1 < n;
+                    if (!(ok = wait1(bar(ctrl->v_full[vs]), (vcnt / C::VSTAGES) & 1, abort, tmo,
+                                         SITE_V_FULL)))
+                        break;
+                    if (jj == 0 && qcnt > 0 &&
+                        !(ok = wait1(bar(ctrl->o_free[0]), (qcnt - 1) & 1, abort, tmo, SITE_O_FREE)))
+                        break;
+                    if (!(ok = wait1(bar(ctrl->p_full[0]), pcnt & 1, abort, tmo, SITE_P_FULL)))
+                        break;
+                    tc_fence_after();
+                    issue_pv(0, vs, jj > 0);
+                    mma_commit(bar(ctrl->o_done[0]));
+                    if (more) {
+                        ks = kcnt % C::KSTAGES;
+                        if (!(ok = wait1(bar(ctrl->k_full[ks]), (kcnt / C::KSTAGES) & 1, abort,
+                                             tmo, SITE_K_FULL)))
+                            break;
+                        tc_fence_after();
+                        issue_s(0, ks);
+                        mma_commit(bar(ctrl->s_full[0]));
+                    }
+                    if (jj == 0 && qcnt > 0 &&
+                        !(ok = wait1(bar(ctrl->o_free[1]), (qcnt - 1) & 1, abort, tmo, SITE_O_FREE)))
+                        break;
+                    if (!(ok = wait1(bar(ctrl->p_full[1]), pcnt & 1, abort, tmo, SITE_P_FULL)))
+                        break;
+                    tc_fence_after();
+                    issue_pv(1, vs, jj > 0);
+                    mma_commit(bar(ctrl->o_done[1]));
+                    mma_commit(bar(ctrl->v_empty[vs]));
+                    ++vcnt;
+                    if (more) {
+                        issue_s(1, ks);
+                        mma_commit(bar(ctrl->s_full[1]));
+                        mma_commit(bar(ctrl->k_empty[ks]));
+                        ++kcnt;
+                        if (jj + 2 == n)
+                            mma_commit(bar(ctrl->q_empty));
+                    }
+                    ++pcnt;
+                }
+                ++qcnt;
+            }
+            // every MMA issued so far completes before TMEM and shared memory go
+            mma_commit(bar(ctrl->final_bar));
+            wait_drain(bar(ctrl->final_bar), 0, tmo);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax
+        const int t = (warp - 4) >> 2;
+        const int qw = warp & 3;
+        const int r = qw * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
+        const uint32_t tS = tmem + lane_off + t * 128;
+        const uint32_t tO = tmem + lane_off + 256 + t * 128;
+        const float sl2 = p.scale_log2;
+        uint32_t scnt = 0, ocnt = 0;
+        bool ok = true;
+        for (int rr = 0; ok; ++rr) {
+            const int u = unit_index(rr, blockIdx.x, gridDim.x);
+            if (u >= p.n_units)
+                break;
+            const RaUnit U = p.units[u];
+            const int bh = t ? U.bh1 : U.bh0;
+            const int ta = t ? U.ta1 : U.ta0;
+            const bool store = (t == 0) || U.tile1_valid;
+            const int a = ta * RA_TILE + r;
+            float m_run = -INFINITY, l_run = 0.f;
+            KvWalk w;
+            w.start(U.rank, max(U.ta0, U.ta1), p);
+            for (int jj = 0; w.valid(); w.advance(), ++jj) {
+                if (!(ok = wait_warp(bar(ctrl->s_full[t]), scnt & 1, abort, tmo, SITE_S_FULL)))
+                    break;
+                ++scnt;
+                if (jj > 0) {
+                    if (!(ok = wait_warp(bar(ctrl->o_done[t]), ocnt & 1, abort, tmo, SITE_O_DONE)))
+                        break;
+                    ++ocnt;
+                }
+                tc_fence_after();
+                const int lim = ra_key_limit(w.cls, a, p.L) - w.tb * RA_TILE;
+                // pass 1: masked row max of the 128 scores
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t x[32];
+                    tmem_ld32(tS + c * 32, x);
+                    tmem_wait_ld();
+                    float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        m0 = fmaxf(m0, c * 32 + e < lim ? __uint_as_float(x[e]) : -INFINITY);
+                        m1 = fmaxf(m1, c * 32 + e + 1 < lim ? __uint_as_float(x[e + 1]) : -INFINITY);
+                    }
+                    mx = fmaxf(mx, fmaxf(m0, m1));
+                }
+                const float m_tile = mx * sl2;  // -inf stays -inf
+                const bool resc = m_tile > m_run + LAZY_RESCALE_LOG2;
+                float alpha = 1.f;
+                if (resc) {
+                    alpha = ex2_approx(m_run - m_tile);  // 0 when m_run = -inf
+                    m_run = m_tile;
+                    l_run *= alpha;
+                }
+                if (jj > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c * 32, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(tO + c * 32, o);
+                    }
+                }
+                // pass 2: P = exp2(s log2e / sqrt(d) - m) as bf16 pairs over
+                // the first 64 columns (chunk c lands on columns already read)
+                const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+                float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t x[32];
+                    tmem_ld32(tS + c * 32, x);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float s0 = c * 32 + 2 * e < lim ? __uint_as_float(x[2 * e]) : -INFINITY;
+                        const float s1 = c * 32 + 2 * e + 1 < lim ? __uint_as_float(x[2 * e + 1]) : -INFINITY;
+                        const float p0 = ex2_approx(fmaf(s0, sl2, neg_m));
+                        const float p1 = ex2_approx(fmaf(s1, sl2, neg_m));
+                        l0 += p0;
+                        l1 += p1;
+                        pk[e] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(tS + c * 16, pk);
+                }
+                l_run += l0 + l1;
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(ctrl->p_full[t]));
+            }
+            if (!ok)
+                break;
+            // ------------------------------------------------ epilogue
+            if (!(ok = wait_warp(bar(ctrl->o_done[t]), ocnt & 1, abort, tmo, SITE_O_DONE)))
+                break;
+            ++ocnt;
+            tc_fence_after();
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            const bool valid = store && a < p.L;
+            const long long orow = (long long)bh * p.S + (long long)U.rank * p.L + a;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                __syncwarp();
+                tmem_ld32(tO + c * 32, o);
+                tmem_wait_ld();
+                if (!valid)
+                    continue;
+                if (p.out_f32) {
+                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + orow * D + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv,
+                                             __uint_as_float(o[4 * e + 1]) * inv,
+                                             __uint_as_float(o[4 * e + 2]) * inv,
+                                             __uint_as_float(o[4 * e + 3]) * inv);
+                } else {
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + orow * D + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        uint4 x;
+                        x.x = pack_bf16x2(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv);
+                        x.y = pack_bf16x2(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
+                        x.z = pack_bf16x2(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
+                        x.w = pack_bf16x2(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
+                        dst[e] = x;
+                    }
+                }
+            }
+            if (valid)
+                p.lse[orow] = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
+            __syncwarp();
+            tc_fence_before();
+            mbar_arrive(bar(ctrl->o_free[t]));
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void *ptr = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+bool encode_rows(CUtensorMap *tm, const void *base, long long rows, int d)
+{
+    auto enc = get_encode_fn();
+    if (!enc)
+        return false;
+    cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+    cuuint32_t box[2] = {64, RA_TILE};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_d(const TcLaunch &a, cudaStream_t st)
+{
+    using C = Cfg<D>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(ra_attn_tc_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess)
+            return e;
+        attr_set = true;
+    }
+    TcParams p;
+    memset(&p, 0, sizeof(p));
+    if (!encode_rows(&p.tm_q, a.q, (long long)a.B * a.H * a.S, D) ||
+        !encode_rows(&p.tm_k, a.k, (long long)a.B * a.Hkv * a.S, D) ||
+        !encode_rows(&p.tm_v, a.v, (long long)a.B * a.Hkv * a.S, D))
+        return cudaErrorInvalidValue;
+    p.units = a.units;
+    p.out = a.out;
+    p.lse = a.lse;
+    p.n_units = a.n_units;
+    p.H = a.H, p.Hkv = a.Hkv, p.S = a.S, p.N = a.N, p.L = a.S / a.N;
+    p.layout = a.layout, p.causal = a.causal;
+    p.s_begin = a.s_begin, p.s_end = a.s_end, p.out_f32 = a.out_f32;
+    p.ntiles = (p.L + RA_TILE - 1) / RA_TILE;
+    p.scale_log2 = 1.4426950408889634f / sqrtf((float)D);
+    p.timeout_ns = a.timeout_ns;
+    if (a.n_units <= 0)
+        return cudaSuccess;
+    const int grid = a.n_units < a.sm_count ? a.n_units : a.sm_count;
+    ra_attn_tc_kernel<D><<<grid, NUM_THREADS, C::SMEM, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_tc(const TcLaunch &a, cudaStream_t st)
+{
+    if (a.d == 128)
+        return launch_d<128>(a, st);
+    if (a.d == 64)
+        return launch_d<64>(a, st);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t read_and_clear_device_status(unsigned int *status)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(status, g_ra_status, sizeof(unsigned int));
+    if (e != cudaSuccess)
+        return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_ra_status, &zero, sizeof(unsigned int));
+}
+
+}  // namespace ra

@@ -1,0 +1,53 @@
+// Internal launchers shared by the C-ABI layer (ra_api.cu) and the kernel
+// translation units.  Not part of the public interface.
+#pragma once
+
+#include <cstddef>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "ra_schedule.h"
+
+namespace ra {
+
+// Status code the device error word carries for a bounded wait that ran out.
+constexpr unsigned int RA_DEV_TIMEOUT_CODE = 5;
+
+void launch_attn_f32(const float *q, const float *k, const float *v, float *out, float *lse,
+                     int B, int H, int Hkv, int S, int d, int N, int layout, int causal,
+                     int s_begin, int s_end, cudaStream_t st);
+
+void launch_permute(const void *src, void *dst, long long rows_total, int S, int N,
+                    long long row_bytes, int inverse, int sm_count, cudaStream_t st);
+
+void launch_merge(float *out_run, float *lse_run, const float *out_s, const float *lse_s,
+                  long long outer, long long stride, long long begin, long long count, int d,
+                  int sm_count, cudaStream_t st);
+
+void launch_finalize(const float *run, const float *run_lse, void *out, float *lse, int out_bf16,
+                     long long rows_total, int S, int N, int striped, int d, int sm_count,
+                     cudaStream_t st);
+
+// Tensor-core attention over a device list of units (see RaUnit).
+struct TcLaunch {
+    const void *q, *k, *v;       // bf16, kernel (possibly striped) order
+    void *out;                   // bf16 (out_f32 = 0) or fp32 normalised partial
+    float *lse;
+    const RaUnit *units;
+    int n_units;
+    int B, H, Hkv, S, d, N;
+    int layout, causal;
+    int s_begin, s_end;          // ring steps walked by every unit
+    int out_f32;
+    unsigned long long timeout_ns;
+    int sm_count;
+};
+
+// Returns cudaSuccess or the first CUDA error met while encoding tensor maps
+// or launching.
+cudaError_t launch_attn_tc(const TcLaunch &a, cudaStream_t st);
+
+// Device-side error word helpers (defined in ra_attn_sm103.cu).
+cudaError_t read_and_clear_device_status(unsigned int *status);
+
+}  // namespace ra

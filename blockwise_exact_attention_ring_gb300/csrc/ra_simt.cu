@@ -1,0 +1,297 @@
+// SIMT kernels of the ring-attention library:
+//   * ra_attn_f32_kernel  exact fp32 ring-ordered attention (no tensor cores)
+//   * ra_permute_kernel   natural <-> striped token order, bit-exact copy
+//   * ra_merge_kernel     running-softmax merge of one ring step's partials
+//   * ra_finalize_kernel  fp32 running result -> output dtype, natural order
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "ra_internal.h"
+#include "ra_schedule.h"
+
+namespace ra {
+
+// ---------------------------------------------------------------- fp32 path
+// One warp per query row.  The warp walks the ring steps s in [s_begin,
+// s_end): key block j = (i - s) mod N, visible keys b < ra_key_limit(...),
+// and keeps the running max m, the running sum l of exp(score - m) and the
+// running weighted values, rescaled whenever m grows ("Ring Attention" page,
+// section "Halka Dikkati Nasil Calisir": running softmax of flash attention,
+// divided at the end).  Lane c owns columns c, c + 32, ...
+constexpr int F32_WARPS = 8;
+constexpr int F32_MAXW = 8;  // d <= 256
+
+__global__ void __launch_bounds__(F32_WARPS * 32)
+ra_attn_f32_kernel(const float *__restrict__ q, const float *__restrict__ k,
+                   const float *__restrict__ v, float *__restrict__ out,
+                   float *__restrict__ lse, int H, int Hkv, int S, int d, int L, int N,
+                   int layout, int causal, int s_begin, int s_end, float scale)
+{
+    const int lane = threadIdx.x & 31;
+    const int a = blockIdx.x * F32_WARPS + (threadIdx.x >> 5);
+    const int i = blockIdx.y;
+    const long long bh = blockIdx.z;
+    if (a >= L)
+        return;
+    const long long b = bh / H;
+    const int h = (int)(bh % H);
+    const long long bhkv = b * Hkv + h / (H / Hkv);
+    const long long qrow = bh * S + (long long)i * L + a;
+    const int nw = (d + 31) / 32;
+
+    float qv[F32_MAXW], acc[F32_MAXW];
+#pragma unroll
+    for (int w = 0; w < F32_MAXW; ++w) {
+        const int c = lane + 32 * w;
+        qv[w] = (w < nw && c < d) ? q[qrow * d + c] * scale : 0.f;
+        acc[w] = 0.f;
+    }
+    float m = -INFINITY, l = 0.f;
+    for (int s = s_begin; s < s_end; ++s) {
+        const int j = ra_ring_block(i, s, N);
+        const int cls = ra_block_class(layout, causal, i, j);
+        if (cls == RA_CLS_SKIP)
+            continue;
+        const int lim = ra_key_limit(cls, a, L);
+        const float *kb = k + (bhkv * S + (long long)j * L) * d;
+        const float *vb = v + (bhkv * S + (long long)j * L) * d;
+        for (int u = 0; u < lim; ++u) {
+            float part = 0.f;
+#pragma unroll
+            for (int w = 0; w < F32_MAXW; ++w) {
+                const int c = lane + 32 * w;
+                if (w < nw && c < d)
+                    part = fmaf(qv[w], kb[(long long)u * d + c], part);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                part += __shfl_xor_sync(0xffffffffu, part, off);
+            const float sc = __shfl_sync(0xffffffffu, part, 0);
+            const float m_new = fmaxf(m, sc);
+            const float corr = expf(m - m_new);  // m = -inf -> 0
+            const float p = expf(sc - m_new);
+            l = fmaf(l, corr, p);
+#pragma unroll
+            for (int w = 0; w < F32_MAXW; ++w) {
+                const int c = lane + 32 * w;
+                if (w < nw && c < d)
+                    acc[w] = fmaf(acc[w], corr, p * vb[(long long)u * d + c]);
+            }
+            m = m_new;
+        }
+    }
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+    for (int w = 0; w < F32_MAXW; ++w) {
+        const int c = lane + 32 * w;
+        if (w < nw && c < d)
+            out[qrow * d + c] = acc[w] * inv;
+    }
+    if (lane == 0)
+        lse[qrow] = l > 0.f ? m + logf(l) : -INFINITY;
+}
+
+void launch_attn_f32(const float *q, const float *k, const float *v, float *out, float *lse,
+                     int B, int H, int Hkv, int S, int d, int N, int layout, int causal,
+                     int s_begin, int s_end, cudaStream_t st)
+{
+    const int L = S / N;
+    dim3 grid((L + F32_WARPS - 1) / F32_WARPS, N, B * H);
+    ra_attn_f32_kernel<<<grid, F32_WARPS * 32, 0, st>>>(
+        q, k, v, out, lse, H, Hkv, S, d, L, N, layout, causal, s_begin, s_end,
+        1.0f / sqrtf((float)d));
+}
+
+// ---------------------------------------------------------------- permute
+// Striped row p = r L + a holds natural token t = a N + r.  Each thread moves
+// one VEC-byte word; the grid walks destination rows, so writes are
+// contiguous and each source row is read whole.
+template <typename VEC>
+__global__ void ra_permute_kernel(const VEC *__restrict__ src, VEC *__restrict__ dst,
+                                  long long n_rows_total, int S, int L, int N,
+                                  int words_per_row, int inverse)
+{
+    const long long n = n_rows_total * words_per_row;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const long long row = idx / words_per_row;
+        const int w = (int)(idx - row * words_per_row);
+        const long long bh = row / S;
+        const int x = (int)(row - bh * S);
+        // forward: x is the striped row p, read natural t(p)
+        // inverse: x is the natural token t, read striped p(t)
+        int other;
+        if (!inverse)
+            other = (x % L) * N + x / L;
+        else
+            other = (x % N) * L + x / N;
+        dst[idx] = src[(bh * S + other) * words_per_row + w];
+    }
+}
+
+void launch_permute(const void *src, void *dst, long long rows_total, int S, int N,
+                    long long row_bytes, int inverse, int sm_count, cudaStream_t st)
+{
+    const int L = S / N;
+    const int threads = 256;
+    auto grid_for = [&](long long n) {
+        long long g = (n + threads - 1) / threads;
+        const long long cap = (long long)sm_count * 8;
+        return (int)(g < cap ? (g > 0 ? g : 1) : cap);
+    };
+    if (row_bytes % 16 == 0) {
+        const int wpr = (int)(row_bytes / 16);
+        ra_permute_kernel<uint4><<<grid_for(rows_total * wpr), threads, 0, st>>>(
+            (const uint4 *)src, (uint4 *)dst, rows_total, S, L, N, wpr, inverse);
+    } else if (row_bytes % 4 == 0) {
+        const int wpr = (int)(row_bytes / 4);
+        ra_permute_kernel<uint32_t><<<grid_for(rows_total * wpr), threads, 0, st>>>(
+            (const uint32_t *)src, (uint32_t *)dst, rows_total, S, L, N, wpr, inverse);
+    } else {
+        const int wpr = (int)row_bytes;
+        ra_permute_kernel<uint8_t><<<grid_for(rows_total * wpr), threads, 0, st>>>(
+            (const uint8_t *)src, (uint8_t *)dst, rows_total, S, L, N, wpr, inverse);
+    }
+}
+
+// ---------------------------------------------------------------- merge
+// Rows are grouped: `outer` groups of `count` rows starting at row `begin`
+// of every group of `stride` rows (for the flat API: outer = 1).  A row is
+// handled by d/4 lanes (16-byte vectors); every lane reads both lse values
+// before the warp synchronises and one lane writes the merged lse.
+__device__ __forceinline__ void merge_weights(float la, float lb, float &wa, float &wb, float &l)
+{
+    const float mx = fmaxf(la, lb);
+    if (mx == -INFINITY) {
+        wa = 0.f, wb = 0.f, l = -INFINITY;
+        return;
+    }
+    const float ea = expf(la - mx), eb = expf(lb - mx);  // -inf -> 0
+    const float sum = ea + eb;
+    l = mx + logf(sum);
+    wa = ea / sum;
+    wb = eb / sum;
+}
+
+__global__ void ra_merge_kernel(float *__restrict__ out_run, float *__restrict__ lse_run,
+                                const float *__restrict__ out_s, const float *__restrict__ lse_s,
+                                long long outer, long long stride, long long begin,
+                                long long count, int d)
+{
+    const int lane = threadIdx.x & 31;
+    const int vpr = d / 4;  // 16-byte vectors per row
+    const int rows_per_warp = vpr >= 32 ? 1 : 32 / vpr;
+    const int vec_per_lane = vpr >= 32 ? (vpr + 31) / 32 : 1;
+    const int sub = vpr >= 32 ? 0 : lane / vpr;  // row within the warp
+    const int lv = vpr >= 32 ? lane : lane % vpr;
+    const long long n_rows = outer * count;
+    const long long warp0 = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+    const long long n_warps = ((long long)gridDim.x * blockDim.x) >> 5;
+    for (long long wr = warp0 * rows_per_warp; wr < n_rows; wr += n_warps * rows_per_warp) {
+        const long long rr = wr + sub;
+        const bool active = sub < rows_per_warp && rr < n_rows;
+        long long row = 0;
+        float la = -INFINITY, lb = -INFINITY;
+        if (active) {
+            const long long o = rr / count;
+            row = o * stride + begin + (rr - o * count);
+            la = lse_run[row];
+            lb = lse_s[row];
+        }
+        float wa, wb, l;
+        merge_weights(la, lb, wa, wb, l);
+        if (active) {
+            float4 *orun = reinterpret_cast<float4 *>(out_run + row * d);
+            const float4 *os = reinterpret_cast<const float4 *>(out_s + row * d);
+            for (int t = 0; t < vec_per_lane; ++t) {
+                const int c = lv + 32 * t;
+                if (c >= vpr)
+                    break;
+                const float4 x = orun[c], y = os[c];
+                float4 r;
+                r.x = wa * x.x + wb * y.x;
+                r.y = wa * x.y + wb * y.y;
+                r.z = wa * x.z + wb * y.z;
+                r.w = wa * x.w + wb * y.w;
+                orun[c] = r;
+            }
+        }
+        __syncwarp();
+        if (active && lv == 0)
+            lse_run[row] = l;
+    }
+}
+
+void launch_merge(float *out_run, float *lse_run, const float *out_s, const float *lse_s,
+                  long long outer, long long stride, long long begin, long long count, int d,
+                  int sm_count, cudaStream_t st)
+{
+    const int threads = 256;
+    const int vpr = d / 4;
+    const int rows_per_warp = vpr >= 32 ? 1 : 32 / vpr;
+    const long long warps = (outer * count + rows_per_warp - 1) / rows_per_warp;
+    long long blocks = (warps + 7) / 8;
+    const long long cap = (long long)sm_count * 8;
+    if (blocks > cap)
+        blocks = cap;
+    if (blocks < 1)
+        blocks = 1;
+    ra_merge_kernel<<<(int)blocks, threads, 0, st>>>(out_run, lse_run, out_s, lse_s, outer,
+                                                     stride, begin, count, d);
+}
+
+// ---------------------------------------------------------------- finalize
+// fp32 running result (kernel order) -> output in natural order; bf16 output
+// is rounded to nearest even.  Striped rows are scattered back to t(p).
+template <typename OUT>
+__global__ void ra_finalize_kernel(const float *__restrict__ run, const float *__restrict__ run_lse,
+                                   OUT *__restrict__ out, float *__restrict__ lse,
+                                   long long rows_total, int S, int L, int N, int striped, int d)
+{
+    const long long n = rows_total * (d / 4);
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const long long row = idx / (d / 4);
+        const int c4 = (int)(idx - row * (d / 4));
+        const long long bh = row / S;
+        const int p = (int)(row - bh * S);
+        const int t = striped ? (p % L) * N + p / L : p;
+        const long long drow = bh * S + t;
+        const float4 x = reinterpret_cast<const float4 *>(run + row * d)[c4];
+        if constexpr (sizeof(OUT) == 4) {
+            reinterpret_cast<float4 *>(out + drow * d)[c4] = x;
+        } else {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(x.z, x.w);
+            uint2 w;
+            w.x = *reinterpret_cast<uint32_t *>(&lo);
+            w.y = *reinterpret_cast<uint32_t *>(&hi);
+            reinterpret_cast<uint2 *>(out + drow * d)[c4] = w;
+        }
+        if (c4 == 0)
+            lse[drow] = run_lse[row];
+    }
+}
+
+void launch_finalize(const float *run, const float *run_lse, void *out, float *lse, int out_bf16,
+                     long long rows_total, int S, int N, int striped, int d, int sm_count,
+                     cudaStream_t st)
+{
+    const int threads = 256;
+    long long blocks = (rows_total * (d / 4) + threads - 1) / threads;
+    const long long cap = (long long)sm_count * 8;
+    if (blocks > cap)
+        blocks = cap;
+    if (blocks < 1)
+        blocks = 1;
+    const int L = S / N;
+    if (out_bf16)
+        ra_finalize_kernel<__nv_bfloat16><<<(int)blocks, threads, 0, st>>>(
+            run, run_lse, (__nv_bfloat16 *)out, lse, rows_total, S, L, N, striped, d);
+    else
+        ra_finalize_kernel<float><<<(int)blocks, threads, 0, st>>>(
+            run, run_lse, (float *)out, lse, rows_total, S, L, N, striped, d);
+}
+
+}  // namespace ra

@@ -1,0 +1,210 @@
+/*
+ * ra.h - C ABI of the GB300 (sm_103a) ring-ordered blockwise exact attention
+ * library (libra.so).
+ *
+ * The method (web pages on ring and context parallelism):
+ *   - "Ring Attention" glossary page (ultralytics.com/tr), section
+ *     "Halka Dikkati Nasil Calisir": the sequence is cut into N blocks, one per
+ *     ring device; every device keeps its query block while key/value blocks
+ *     travel round the ring, so at step s device i meets key/value block
+ *     j = (i - s) mod N; partial results are combined with the running softmax
+ *     of flash attention (running max, running sum of exponentiated scores,
+ *     running score-weighted values, divided at the end); under a causal mask
+ *     devices holding early query blocks skip most key blocks, and striped
+ *     attention spreads every device's tokens evenly along the sequence to
+ *     balance that work.
+ *   - "Context Parallelism" glossary page (ultralytics.com/tr), section
+ *     "Pratik Kullanim ve Odunlesimler": tensors are [batch, heads, sequence,
+ *     dim] with the sequence on dim 2, causal scaled-dot-product attention,
+ *     output in the input dtype.
+ *   - The same page, section "Baglam Paralelligi Nasil Calisir?": the result
+ *     equals full-sequence attention up to ordinary rounding differences.
+ *
+ * Here the N ring ranks are emulated on one GPU: rank r is an index range of
+ * the same HBM buffers, and "receiving block j" is reading it in place.
+ *
+ * Common conventions for every entry point
+ *   - Tensors are dense, row-major, C-contiguous, in NATURAL token order:
+ *       q   [B, H,   S, d]        k, v [B, Hkv, S, d]
+ *       out [B, H,   S, d]        lse  [B, H,   S]   (fp32, natural log)
+ *   - Query head h reads kv head h / (H / Hkv) (grouped-query attention).
+ *   - Scores are scaled by 1/sqrt(d).  Causal: key u is visible to query t iff
+ *     u <= t in natural positions.  lse = ln sum_u exp(q_t . k_u / sqrt(d)).
+ *   - Block length L = S / n_blocks; S must be a multiple of n_blocks.
+ *   - layout RA_LAYOUT_CONTIGUOUS: rank r owns tokens [r L, (r + 1) L).
+ *     layout RA_LAYOUT_STRIPED: rank r owns tokens t with t mod N == r, in
+ *     increasing t (striped attention).
+ *   - Pointers are DEVICE pointers owned by the caller, 16-byte aligned, and
+ *     stay valid until the enqueued work has finished.  `out` and `lse` must
+ *     not overlap any input.
+ *   - Every call is asynchronous on `stream` (NULL = legacy default stream):
+ *     it validates its arguments, enqueues kernels and returns.  A status
+ *     other than RA_OK means nothing was enqueued and nothing was written.
+ *     Errors raised later on the device (a bounded wait that ran out) are
+ *     reported by ra_check().
+ *   - No C++ exception crosses this interface.  The library reads no
+ *     environment variables.
+ */
+#ifndef RA_H_
+#define RA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Identical to cudaStream_t; declared here so callers need no CUDA headers. */
+typedef struct CUstream_st *ra_stream_t;
+
+typedef enum {
+    RA_OK = 0,
+    RA_ERR_INVALID_ARG = 1,  /* bad sizes, null/misaligned/overlapping pointers */
+    RA_ERR_UNSUPPORTED = 2,  /* valid request outside this build's kernels    */
+    RA_ERR_CUDA = 3,         /* a CUDA runtime call failed                     */
+    RA_ERR_NO_MEMORY = 4,    /* scratch allocation failed                      */
+    RA_ERR_TIMEOUT = 5,      /* a device-side bounded wait ran out             */
+    RA_ERR_WORKSPACE = 6     /* caller workspace too small or misaligned       */
+} ra_status;
+
+typedef enum { RA_LAYOUT_CONTIGUOUS = 0, RA_LAYOUT_STRIPED = 1 } ra_layout;
+
+/* RA_MODE_FUSED: one persistent launch walks, for every query tile, the key
+ *   blocks in ring order and keeps the running softmax on chip.
+ * RA_MODE_PER_STEP: one launch per ring step s writes that step's partial
+ *   (out_s, lse_s) for every rank, then ra_merge-style merging folds it into
+ *   the running result, as each ring device would after receiving a block. */
+typedef enum { RA_MODE_FUSED = 0, RA_MODE_PER_STEP = 1 } ra_mode;
+
+typedef enum { RA_DTYPE_BF16 = 0, RA_DTYPE_F32 = 1 } ra_dtype;
+
+/*
+ * ra_forward - ring-ordered blockwise exact attention, bf16 in, bf16 out.
+ * Source: "Ring Attention" page, section "Halka Dikkati Nasil Calisir" (ring
+ * schedule, running-softmax merge, causal block skipping, striping).
+ * q, k, v, out: bf16 (raw 16-bit storage); lse: fp32.  Computes in fp32 with
+ * bf16 operands on the tensor cores; out is rounded to bf16 (nearest even).
+ * Supported: d in {64, 128}; any block length L >= 1.  Uses RA_MODE_FUSED and
+ * allocates its scratch stream-ordered (cudaMallocAsync on `stream`).
+ * Returns RA_ERR_INVALID_ARG for B, H, Hkv, S, n_blocks < 1, H % Hkv != 0,
+ * S % n_blocks != 0, layout not in ra_layout, null, misaligned or overlapping
+ * pointers; RA_ERR_UNSUPPORTED for other d.
+ */
+ra_status ra_forward(const void *q, const void *k, const void *v, void *out, float *lse,
+                     int B, int H, int Hkv, int S, int d, int n_blocks,
+                     int layout, int causal, ra_stream_t stream);
+
+/*
+ * ra_forward_f32 - the same computation for fp32 tensors, fp32 arithmetic
+ * throughout (no TF32, no reduced-precision operands), for exact checks such
+ * as the pages' 4-device, block-8, dim-16 simulation ("Ring Attention" page,
+ * section "Halka Dikkati Nasil Calisir", the four-device example).
+ * Supported: 1 <= d <= 256, any L >= 1.  Same error rules as ra_forward.
+ */
+ra_status ra_forward_f32(const float *q, const float *k, const float *v, float *out,
+                         float *lse, int B, int H, int Hkv, int S, int d, int n_blocks,
+                         int layout, int causal, ra_stream_t stream);
+
+/*
+ * ra_workspace_bytes - bytes of scratch ra_forward_ws needs for this problem
+ * (striped copies of q, k, v, out and lse; per-step running and partial
+ * results).  0 when none is needed (bf16 contiguous fused).
+ * dtype is a ra_dtype, mode a ra_mode.  Returns 0 for an invalid request.
+ */
+size_t ra_workspace_bytes(int B, int H, int Hkv, int S, int d, int n_blocks, int layout,
+                          int causal, int mode, int dtype);
+
+/*
+ * ra_forward_ws - ra_forward / ra_forward_f32 with an explicit mode and a
+ * caller-owned device workspace `ws` of `ws_bytes` bytes (256-byte aligned,
+ * at least ra_workspace_bytes(...)); no per-call allocation.  dtype selects the
+ * tensor type (RA_DTYPE_BF16: q, k, v, out bf16; RA_DTYPE_F32: all fp32).
+ * RA_ERR_WORKSPACE if ws is null, misaligned or too small.  Calls sharing one
+ * workspace must be ordered on the GPU (same stream or events).
+ * Every bf16 entry point keeps, per device and problem shape, the ring-step
+ * schedule (the tensor-core kernel's work list) in device memory: the first
+ * call for a shape builds it on the host and copies it with one cudaMalloc
+ * and one synchronous cudaMemcpy; it lives until the process exits.
+ */
+ra_status ra_forward_ws(const void *q, const void *k, const void *v, void *out, float *lse,
+                        int B, int H, int Hkv, int S, int d, int n_blocks, int layout,
+                        int causal, int dtype, int mode, void *ws, size_t ws_bytes,
+                        ra_stream_t stream);
+
+/*
+ * ra_forward_rank_major - ra_forward_ws for tensors already stored in the
+ * layout's rank-major order: rank 0's L tokens, then rank 1's, and so on
+ * (for RA_LAYOUT_STRIPED, row p = r L + a holds natural token a N + r; for
+ * RA_LAYOUT_CONTIGUOUS this is the natural order).  q, k, v, out and lse all
+ * use that order and no permutation is launched, as for a model that keeps
+ * its activations striped from embedding to output.  Same arguments, types
+ * and error rules as ra_forward_ws; the workspace is needed only for
+ * RA_MODE_PER_STEP (ra_workspace_bytes of the contiguous layout).
+ * Source: "Ring Attention" page, section "Halka Dikkati Nasil Calisir".
+ */
+ra_status ra_forward_rank_major(const void *q, const void *k, const void *v, void *out,
+                                float *lse, int B, int H, int Hkv, int S, int d, int n_blocks,
+                                int layout, int causal, int dtype, int mode, void *ws,
+                                size_t ws_bytes, ra_stream_t stream);
+
+/*
+ * ra_permute - move the sequence axis between natural and striped order.
+ * Source: "Ring Attention" page, section "Halka Dikkati Nasil Calisir"
+ * (striped attention).  With L = S / n_blocks, striped row p = r L + a holds
+ * natural token t = a n_blocks + r.  src and dst are [B * Hn, S, row] with
+ * row = d * elem_bytes bytes; inverse = 0 gathers natural -> striped
+ * (dst[p] = src[t(p)]), inverse = 1 scatters back (dst[t(p)] = src[p]).
+ * Bit-exact copy; elem_bytes in {1, 2, 4, 8}; src and dst must not overlap.
+ */
+ra_status ra_permute(const void *src, void *dst, int B, int Hn, int S, int d, int elem_bytes,
+                     int n_blocks, int inverse, ra_stream_t stream);
+
+/*
+ * ra_merge - fold one ring step's partial result into the running one.
+ * Source: "Ring Attention" page, section "Halka Dikkati Nasil Calisir"
+ * (partial results combined with the running softmax of flash attention).
+ * Per row: lse = ln(e^lse_run + e^lse_s);
+ *          out_run = e^(lse_run - lse) out_run + e^(lse_s - lse) out_s;
+ *          lse_run = lse.
+ * A side with lse = -inf (no visible key) contributes nothing; if both are
+ * -inf the row stays out 0, lse -inf.  out_run, out_s: fp32 [rows, d];
+ * lse_run, lse_s: fp32 [rows].  1 <= d <= 256, d % 4 == 0 (16-byte vectors).
+ */
+ra_status ra_merge(float *out_run, float *lse_run, const float *out_s, const float *lse_s,
+                   long long rows, int d, ra_stream_t stream);
+
+/*
+ * ra_check - synchronise `stream`, then read and clear the device error word
+ * that bounded waits set.  RA_OK, RA_ERR_TIMEOUT, or RA_ERR_CUDA when the
+ * stream reported a CUDA error.
+ */
+ra_status ra_check(ra_stream_t stream);
+
+/* Human-readable name of a ra_status value; never NULL. */
+const char *ra_status_string(int status);
+
+/* Number of CUDA kernels this library has launched in the process so far
+ * (all entry points, all devices).  Lets a caller count the launches inside
+ * a timed region. */
+unsigned long long ra_launch_count(void);
+
+/* Library version string, e.g. "ra 0.1.0 sm_103a". */
+const char *ra_version(void);
+
+/*
+ * ra_schedule_stats - host-only view of the ring-step scheduler, no GPU
+ * needed.  For layout, causal, n_blocks and block length L, writes for every
+ * (rank i, step s) the number of visible (query, key) pairs that rank i
+ * computes at step s into pairs[i * n_blocks + s], and the number of
+ * 128 x 128 tiles it launches into tiles[i * n_blocks + s] (either array may
+ * be NULL).  Returns the total number of visible pairs, or -1 on bad input.
+ */
+long long ra_schedule_stats(int layout, int causal, int n_blocks, int L,
+                            long long *pairs, long long *tiles);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RA_H_ */

@@ -1,0 +1,91 @@
+"""Host-side checks of the C-ABI library: it loads without a GPU, exports every
+function include/ra.h declares, and rejects invalid requests before touching
+the device (no compute call is made here)."""
+import ctypes
+
+import pytest
+
+import blockwise_exact_attention_ring_gb300 as ra
+from blockwise_exact_attention_ring_gb300 import binding as rb
+
+
+def test_library_exports_every_declared_symbol():
+    L = ra.lib()
+    names = rb.header_functions()
+    assert {"ra_forward", "ra_forward_f32", "ra_forward_ws", "ra_workspace_bytes", "ra_permute",
+            "ra_merge", "ra_check", "ra_status_string", "ra_version",
+            "ra_schedule_stats"} <= set(names)
+    for n in names:
+        assert getattr(L, n) is not None
+
+
+def test_status_strings_and_version():
+    assert ra.status_string(0) == "RA_OK"
+    assert ra.status_string(1) == "RA_ERR_INVALID_ARG"
+    assert ra.status_string(5) == "RA_ERR_TIMEOUT"
+    assert ra.status_string(99) == "RA_ERR_UNKNOWN"
+    assert "sm_103a" in ra.version()
+
+
+# Fake, 16-byte aligned, non-overlapping "device" addresses: validation runs
+# on the host and must reject these requests before any CUDA call.
+Q, K, V, OUT, LSE = (ctypes.c_void_p(0x10000000 * (i + 1)) for i in range(5))
+
+
+def _fwd(B=1, H=4, Hkv=2, S=256, d=128, N=2, layout=0, causal=1, q=Q, out=OUT, lse=LSE):
+    return ra.lib().ra_forward(q, K, V, out, lse, B, H, Hkv, S, d, N, layout, causal, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(B=0), rb.RA_ERR_INVALID_ARG),
+    (dict(H=3), rb.RA_ERR_INVALID_ARG),            # H % Hkv != 0
+    (dict(S=255), rb.RA_ERR_INVALID_ARG),          # S % n_blocks != 0
+    (dict(N=0), rb.RA_ERR_INVALID_ARG),
+    (dict(layout=2), rb.RA_ERR_INVALID_ARG),
+    (dict(causal=3), rb.RA_ERR_INVALID_ARG),
+    (dict(d=96), rb.RA_ERR_UNSUPPORTED),           # tensor-core path: d in {64, 128}
+    (dict(q=ctypes.c_void_p(0x10000008)), rb.RA_ERR_INVALID_ARG),  # misaligned
+    (dict(q=ctypes.c_void_p(0)), rb.RA_ERR_INVALID_ARG),           # null
+    (dict(out=ctypes.c_void_p(0x10000000 + 4096)), rb.RA_ERR_INVALID_ARG),  # out overlaps q
+    (dict(lse=ctypes.c_void_p(0x40000000 + 64)), rb.RA_ERR_INVALID_ARG),   # lse overlaps out
+])
+def test_forward_rejects_invalid_requests(kw, expect):
+    assert _fwd(**kw) == expect
+
+
+def test_f32_and_ws_validation():
+    L = ra.lib()
+    assert L.ra_forward_f32(Q, K, V, OUT, LSE, 1, 1, 1, 32, 300, 4, 0, 0, None) == rb.RA_ERR_UNSUPPORTED
+    assert L.ra_forward_f32(Q, K, V, OUT, LSE, 1, 1, 1, 30, 16, 4, 0, 0, None) == rb.RA_ERR_INVALID_ARG
+    # striped needs a workspace: null workspace is rejected before any launch
+    assert L.ra_forward_ws(Q, K, V, OUT, LSE, 1, 4, 2, 256, 128, 2, 1, 1, 0, 0, None, 0,
+                           None) == rb.RA_ERR_WORKSPACE
+    # misaligned workspace
+    assert L.ra_forward_ws(Q, K, V, OUT, LSE, 1, 4, 2, 256, 128, 2, 1, 1, 0, 0,
+                           ctypes.c_void_p(0x50000010), 1 << 30, None) == rb.RA_ERR_WORKSPACE
+    # bad mode / dtype
+    assert L.ra_forward_ws(Q, K, V, OUT, LSE, 1, 4, 2, 256, 128, 2, 0, 1, 0, 7, None, 0,
+                           None) == rb.RA_ERR_INVALID_ARG
+    assert L.ra_forward_ws(Q, K, V, OUT, LSE, 1, 4, 2, 256, 128, 2, 0, 1, 5, 0, None, 0,
+                           None) == rb.RA_ERR_INVALID_ARG
+
+
+def test_workspace_sizes():
+    B, H, Hkv, S, d, N = 1, 4, 2, 512, 128, 4
+    # contiguous fused bf16 needs no scratch at all
+    assert ra.workspace_bytes(B, H, Hkv, S, d, N, "contiguous", True, "fused") == 0
+    striped = ra.workspace_bytes(B, H, Hkv, S, d, N, "striped", True, "fused")
+    # q', k', v', out' (bf16) and lse' (fp32), each 256-byte aligned
+    assert striped == 2 * (B * H * S * d) * 2 + 2 * (B * Hkv * S * d) * 2 + B * H * S * 4
+    per_step = ra.workspace_bytes(B, H, Hkv, S, d, N, "contiguous", True, "per_step")
+    assert per_step == 2 * (B * H * S * d * 4 + B * H * S * 4)
+    assert ra.workspace_bytes(B, 3, 2, S, d, N) == 0  # invalid request -> 0
+
+
+def test_permute_and_merge_validation():
+    L = ra.lib()
+    assert L.ra_permute(Q, K, 1, 1, 30, 8, 2, 4, 0, None) == rb.RA_ERR_INVALID_ARG   # S % N
+    assert L.ra_permute(Q, K, 1, 1, 32, 8, 3, 4, 0, None) == rb.RA_ERR_INVALID_ARG   # elem size
+    assert L.ra_permute(Q, Q, 1, 1, 32, 8, 2, 4, 0, None) == rb.RA_ERR_INVALID_ARG   # in place
+    assert L.ra_merge(Q, K, V, OUT, 10, 6, None) == rb.RA_ERR_INVALID_ARG           # d % 4
+    assert L.ra_merge(Q, K, Q, OUT, 10, 8, None) == rb.RA_ERR_INVALID_ARG           # aliasing

@@ -1,0 +1,67 @@
+"""The host ring-step scheduler against the causal rule written out on natural
+token positions (brute force over every (query, key) pair)."""
+import itertools
+
+import numpy as np
+import pytest
+
+import blockwise_exact_attention_ring_gb300 as ra
+import oracle
+
+
+def _brute_pairs(layout, causal, N, L):
+    """pairs[i, s]: visible (query, key) pairs rank i meets at ring step s,
+    counted from natural positions (t of query, u of key)."""
+    S = N * L
+    if layout == "striped":
+        order = oracle.stripe_order(S, N)          # striped row -> natural token
+    else:
+        order = np.arange(S)
+    pos = order.reshape(N, L)                        # pos[rank, local] = natural token
+    out = np.zeros((N, N), dtype=np.int64)
+    for i in range(N):
+        for s in range(N):
+            j = (i - s) % N                          # block that reached rank i at step s
+            t = pos[i][:, None]
+            u = pos[j][None, :]
+            out[i, s] = int((u <= t).sum()) if causal else L * L
+    return out
+
+
+@pytest.mark.parametrize("layout,causal,N,L", list(itertools.product(
+    ["contiguous", "striped"], [False, True], [1, 2, 3, 4, 8], [1, 5, 8, 130])))
+def test_pairs_per_rank_and_step_match_brute_force(layout, causal, N, L):
+    total, pairs, tiles = ra.schedule_stats(layout, causal, N, L)
+    assert np.array_equal(pairs, _brute_pairs(layout, causal, N, L))
+    S = N * L
+    assert total == (S * (S + 1) // 2 if causal else S * S)
+    ntiles = -(-L // 128)
+    # no visible pair is ever left out of the launched tiles
+    assert np.all(tiles * 128 * 128 >= pairs)
+    assert np.all(tiles <= ntiles * ntiles)
+
+
+@pytest.mark.parametrize("S,expect", [(32768, 536887296), (262144, 34359869440),
+                                      (1048576, 549756338176)])
+def test_causal_pair_totals_at_workload_sizes(S, expect):
+    # S(S+1)/2 for the 32K, 256K and 1M causal workloads
+    assert S * (S + 1) // 2 == expect
+    for layout, N in (("contiguous", 4), ("striped", 8)):
+        if S // N > 40000:
+            continue  # the per-row loop is O(N^2 L); the closed form above covers it
+        total, _, _ = ra.schedule_stats(layout, True, N, S // N)
+        assert total == expect
+
+
+def test_striping_balances_causal_work():
+    """Critical path sum_s max_i work(i, s): striping cuts it toward the mean;
+    contiguous causal rank i idles for the steps s > i."""
+    N, L = 8, 1024
+    _, pc, _ = ra.schedule_stats("contiguous", True, N, L)
+    _, ps, _ = ra.schedule_stats("striped", True, N, L)
+    assert pc.sum() == ps.sum()
+    assert np.count_nonzero(pc == 0) == N * (N - 1) // 2      # skipped block pairs
+    assert np.count_nonzero(ps == 0) == 0                     # striped skips none
+    crit_c = pc.max(axis=0).sum()   # L^2/2 + (N - 1) L^2
+    crit_s = ps.max(axis=0).sum()   # N L (L + 1) / 2
+    assert abs(crit_c / crit_s - (N - 0.5) / (N / 2)) < 0.01
