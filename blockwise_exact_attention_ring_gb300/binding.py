@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(HERE, "libra.so")
 HEADER = os.path.join(HERE, "..", "include", "ra.h")
 
 RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA = 0, 1, 2, 3
-RA_ERR_NO_MEMORY, RA_ERR_TIMEOUT, RA_ERR_WORKSPACE = 4, 5, 6
+RA_ERR_NO_MEMORY, RA_ERR_TIMEOUT, RA_ERR_WORKSPACE, RA_ERR_SCRATCH_LIMIT = 4, 5, 6, 7
 LAYOUTS = {"contiguous": 0, "striped": 1}
 MODES = {"fused": 0, "per_step": 1}
 DTYPES = {torch.bfloat16: 0, torch.float32: 1}
@@ -50,6 +50,7 @@ def lib():
     vp, i, ll, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_size_t
     L.ra_forward.argtypes = [vp] * 5 + [i] * 8 + [vp]
     L.ra_forward_f32.argtypes = [vp] * 5 + [i] * 8 + [vp]
+    L.ra_forward_noalloc.argtypes = [vp] * 5 + [i] * 8 + [vp]
     L.ra_workspace_bytes.argtypes = [i] * 10
     L.ra_workspace_bytes.restype = sz
     L.ra_forward_ws.argtypes = [vp] * 5 + [i] * 10 + [vp, sz, vp]
@@ -61,7 +62,8 @@ def lib():
     L.ra_version.restype = ctypes.c_char_p
     L.ra_schedule_stats.argtypes = [i, i, i, i, vp, vp]
     L.ra_schedule_stats.restype = ll
-    for fn in ("ra_forward", "ra_forward_f32", "ra_forward_ws", "ra_permute", "ra_merge", "ra_check"):
+    for fn in ("ra_forward", "ra_forward_f32", "ra_forward_noalloc", "ra_forward_ws", "ra_permute",
+               "ra_merge", "ra_check"):
         getattr(L, fn).restype = i
     _lib = L
     return L

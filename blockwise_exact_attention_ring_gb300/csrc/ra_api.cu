@@ -377,6 +377,7 @@ ra_status ra_forward_rank_major(const void *q, const void *k, const void *v, voi
 
 unsigned long long ra_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+
 ra_status ra_permute(const void *src, void *dst, int B, int Hn, int S, int d, int elem_bytes, int n_blocks,
                      int inverse, ra_stream_t stream)
 {
@@ -441,6 +442,7 @@ const char *ra_status_string(int status)
     case RA_ERR_NO_MEMORY: return "RA_ERR_NO_MEMORY";
     case RA_ERR_TIMEOUT: return "RA_ERR_TIMEOUT";
     case RA_ERR_WORKSPACE: return "RA_ERR_WORKSPACE";
+    case RA_ERR_SCRATCH_LIMIT: return "RA_ERR_SCRATCH_LIMIT";
     default: return "RA_ERR_UNKNOWN";
     }
 }
@@ -471,3 +473,114 @@ long long ra_schedule_stats(int layout, int causal, int n_blocks, int L, long lo
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ no-alloc variant
+// ra_forward for callers that cannot allocate device memory (see include/ra.h):
+// all scratch lives in one fixed device array that is part of the library's
+// image, so nothing is allocated per call or per shape.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[RA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device with that device current.  In host code the array's name is only
+// a host-side stand-in, never a device address.
+ra_status noalloc_scratch(void **ptr)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return RA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return RA_ERR_CUDA;
+        }
+        g_noalloc_ptr[dev] = p;
+    }
+    *ptr = g_noalloc_ptr[dev];
+    return RA_OK;
+}
+
+}  // namespace
+
+extern "C" ra_status ra_forward_noalloc(const void *q, const void *k, const void *v, void *out, float *lse,
+                                        int B, int H, int Hkv, int S, int d, int n_blocks, int layout,
+                                        int causal, ra_stream_t stream)
+{
+    const Problem p{B, H, Hkv, S, d, n_blocks, layout, causal, RA_DTYPE_BF16, RA_MODE_FUSED};
+    ra_status rs = check_problem(p);
+    if (rs != RA_OK)
+        return rs;
+    if (!q || !k || !v || !out || !lse)
+        return RA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+        return RA_ERR_INVALID_ARG;
+    const size_t qb = p.q_elems() * p.esz(), kvb = p.kv_elems() * p.esz(), lb = p.rows() * 4;
+    for (const void *in : {q, k, v})
+        if (overlaps(out, qb, in, in == q ? qb : kvb) || overlaps(lse, lb, in, in == q ? qb : kvb))
+            return RA_ERR_INVALID_ARG;
+    if (overlaps(out, qb, lse, lb))
+        return RA_ERR_INVALID_ARG;
+
+    // scratch: [work list][striped q', k', v', out', lse'], 256-byte aligned
+    const std::vector<RaUnit> units = build_units(B, H, Hkv, S, n_blocks, layout, causal, 0, n_blocks);
+    const bool striped = layout == RA_LAYOUT_STRIPED;
+    const size_t units_bytes = align256(units.size() * sizeof(RaUnit));
+    const size_t off_q = units_bytes, off_k = off_q + align256(qb), off_v = off_k + align256(kvb);
+    const size_t off_o = off_v + align256(kvb), off_l = off_o + align256(qb);
+    const size_t need = striped ? off_l + align256(lb) : units_bytes;
+    if (need > RA_NOALLOC_SCRATCH_BYTES)
+        return RA_ERR_SCRATCH_LIMIT;
+
+    void *scratch = nullptr;
+    if ((rs = noalloc_scratch(&scratch)) != RA_OK)
+        return rs;
+    char *base = static_cast<char *>(scratch);
+    cudaStream_t st = (cudaStream_t)stream;
+    if (!units.empty() && cudaMemcpyAsync(base, units.data(), units.size() * sizeof(RaUnit),
+                                          cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return RA_ERR_CUDA;
+
+    const int sm = sm_count_current();
+    const long long row_bytes = (long long)d * 2;
+    const void *qk = q, *kk = k, *vk = v;
+    void *ok_out = out;
+    float *ok_lse = lse;
+    if (striped) {
+        ra::launch_permute(q, base + off_q, (long long)B * H * S, S, n_blocks, row_bytes, 0, sm, st);
+        ra::launch_permute(k, base + off_k, (long long)B * Hkv * S, S, n_blocks, row_bytes, 0, sm, st);
+        ra::launch_permute(v, base + off_v, (long long)B * Hkv * S, S, n_blocks, row_bytes, 0, sm, st);
+        count_launch(3);
+        if (cudaGetLastError() != cudaSuccess)
+            return RA_ERR_CUDA;
+        qk = base + off_q, kk = base + off_k, vk = base + off_v;
+        ok_out = base + off_o;
+        ok_lse = (float *)(base + off_l);
+    }
+    ra::TcLaunch a{};
+    a.q = qk, a.k = kk, a.v = vk, a.out = ok_out, a.lse = ok_lse;
+    a.units = reinterpret_cast<const RaUnit *>(base), a.n_units = (int)units.size();
+    a.B = B, a.H = H, a.Hkv = Hkv, a.S = S, a.d = d, a.N = n_blocks;
+    a.layout = layout, a.causal = causal, a.s_begin = 0, a.s_end = n_blocks;
+    a.out_f32 = 0;
+    a.timeout_ns = g_timeout_ns;
+    a.sm_count = sm;
+    if (a.n_units > 0)
+        count_launch();
+    if (ra::launch_attn_tc(a, st) != cudaSuccess)
+        return RA_ERR_CUDA;
+    if (striped) {
+        ra::launch_permute(ok_out, out, (long long)p.rows(), S, n_blocks, row_bytes, 1, sm, st);
+        ra::launch_permute(ok_lse, lse, (long long)p.rows(), S, n_blocks, 4, 1, sm, st);
+        count_launch(2);
+        if (cudaGetLastError() != cudaSuccess)
+            return RA_ERR_CUDA;
+    }
+    return RA_OK;
+}

@@ -65,7 +65,9 @@ typedef enum {
     RA_ERR_CUDA = 3,         /* a CUDA runtime call failed                     */
     RA_ERR_NO_MEMORY = 4,    /* scratch allocation failed                      */
     RA_ERR_TIMEOUT = 5,      /* a device-side bounded wait ran out             */
-    RA_ERR_WORKSPACE = 6     /* caller workspace too small or misaligned       */
+    RA_ERR_WORKSPACE = 6,    /* caller workspace too small or misaligned       */
+    RA_ERR_SCRATCH_LIMIT = 7 /* problem needs more than the library's fixed
+                                scratch array (ra_forward_noalloc only)        */
 } ra_status;
 
 typedef enum { RA_LAYOUT_CONTIGUOUS = 0, RA_LAYOUT_STRIPED = 1 } ra_layout;
@@ -147,6 +149,45 @@ ra_status ra_forward_rank_major(const void *q, const void *k, const void *v, voi
                                 float *lse, int B, int H, int Hkv, int S, int d, int n_blocks,
                                 int layout, int causal, int dtype, int mode, void *ws,
                                 size_t ws_bytes, ra_stream_t stream);
+
+/*
+ * ra_forward_noalloc - ra_forward for callers that cannot allocate device
+ * memory.  No counterpart on the pages: this is a deployment variant of the
+ * same computation, with the same arguments, result and error rules as
+ * ra_forward (bf16, fused ring, natural token order).
+ *
+ * Who needs it: code that runs under a memory manager that owns every byte
+ * of device memory (a framework's caching allocator or an inference server
+ * that reserves its whole budget at start-up and forbids allocation after
+ * that), and latency-critical loops that must not meet an allocation-time
+ * synchronisation or an out-of-memory failure half way through.  ra_forward
+ * gets its scratch with cudaMallocAsync and keeps each problem shape's
+ * schedule in memory it cudaMallocs once; this entry point does neither.
+ *
+ * Its scratch (the schedule's work list and, for RA_LAYOUT_STRIPED, the
+ * striped copies of q, k, v, out and lse) lives in one fixed array of
+ * RA_NOALLOC_SCRATCH_BYTES (64 MiB) that is part of the library's device
+ * image: every GPU that loads the library holds it until the process exits.
+ * A problem whose scratch would not fit returns RA_ERR_SCRATCH_LIMIT and
+ * enqueues nothing; contiguous problems need only the work list (32 bytes per
+ * pair of 128-row query tiles), striped ones also 2 (B H + 2 B Hkv) S d + 4 B H S
+ * bytes.  Nothing in the array has to start at zero: every byte a call reads
+ * was written earlier by the same call.
+ *
+ * All calls on a device share the one array and it keeps the last call's
+ * contents, so calls that can overlap on the GPU (different streams without
+ * ordering between them) race: order them on one stream or with events.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  The work list is copied in with
+ * cudaMemcpyAsync from pageable host memory, which the driver stages before
+ * returning.  Calls no cudaMalloc, cudaMallocAsync, cudaFree or other
+ * allocating routine.
+ */
+#define RA_NOALLOC_SCRATCH_BYTES (64ull << 20)
+ra_status ra_forward_noalloc(const void *q, const void *k, const void *v, void *out, float *lse,
+                             int B, int H, int Hkv, int S, int d, int n_blocks, int layout,
+                             int causal, ra_stream_t stream);
 
 /*
  * ra_permute - move the sequence axis between natural and striped order.
