@@ -60,6 +60,11 @@ def lib():
     L.ra_status_string.argtypes = [i]
     L.ra_status_string.restype = ctypes.c_char_p
     L.ra_version.restype = ctypes.c_char_p
+    L.ra_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
+    L.ra_set_wait_timeout_ns.restype = None
+    L.ra_wait_probe.argtypes = [ctypes.c_ulonglong, vp]
+    L.ra_wait_probe.restype = i
+    L.ra_launch_count.restype = ctypes.c_ulonglong
     L.ra_schedule_stats.argtypes = [i, i, i, i, vp, vp]
     L.ra_schedule_stats.restype = ll
     for fn in ("ra_forward", "ra_forward_f32", "ra_forward_noalloc", "ra_forward_ws", "ra_permute",

@@ -377,6 +377,18 @@ ra_status ra_forward_rank_major(const void *q, const void *k, const void *v, voi
 
 unsigned long long ra_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+void ra_set_wait_timeout_ns(unsigned long long timeout_ns)
+{
+    g_timeout_ns = timeout_ns ? timeout_ns : kDefaultTimeoutNs;
+}
+
+ra_status ra_wait_probe(unsigned long long timeout_ns, ra_stream_t stream)
+{
+    if (timeout_ns < 1000000ull || timeout_ns > 10000000000ull)
+        return RA_ERR_INVALID_ARG;
+    count_launch();
+    return ra::launch_wait_probe(timeout_ns, (cudaStream_t)stream) == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+}
 
 ra_status ra_permute(const void *src, void *dst, int B, int Hn, int S, int d, int elem_bytes, int n_blocks,
                      int inverse, ra_stream_t stream)

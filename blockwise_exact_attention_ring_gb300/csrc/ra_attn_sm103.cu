@@ -52,7 +52,7 @@ constexpr float LN2 = 0.693147180559945309f;
 
 enum Site : unsigned int {
     SITE_Q_EMPTY = 1, SITE_K_EMPTY, SITE_V_EMPTY, SITE_Q_FULL, SITE_K_FULL, SITE_V_FULL,
-    SITE_P_FULL, SITE_O_FREE, SITE_S_FULL, SITE_O_DONE, SITE_FINAL, SITE_DRAIN
+    SITE_P_FULL, SITE_O_FREE, SITE_S_FULL, SITE_O_DONE, SITE_FINAL, SITE_DRAIN, SITE_PROBE
 };
 
 template <int D>
@@ -164,6 +164,73 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
           "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
           "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
+}
+
+// Row max of one thread's 128 scores in TMEM (4 loads of 32 columns), with
+// columns at or past `lim` treated as -inf when MASK.  Two max3 chains.
+template <bool MASK>
+__device__ __forceinline__ float row_max(uint32_t tS, int lim)
+{
+    float ma = -INFINITY, mb = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t x[32];
+        tmem_ld32(tS + c * 32, x);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+            float v0 = __uint_as_float(x[e]), v1 = __uint_as_float(x[e + 1]);
+            float v2 = __uint_as_float(x[e + 2]), v3 = __uint_as_float(x[e + 3]);
+            if (MASK) {
+                const int col = c * 32 + e;
+                v0 = col < lim ? v0 : -INFINITY;
+                v1 = col + 1 < lim ? v1 : -INFINITY;
+                v2 = col + 2 < lim ? v2 : -INFINITY;
+                v3 = col + 3 < lim ? v3 : -INFINITY;
+            }
+            ma = max3f(ma, v0, v1);
+            mb = max3f(mb, v2, v3);
+        }
+    }
+    return fmaxf(ma, mb);
+}
+
+// P = exp2(s * sl2 + neg_m) for the 128 scores, packed to bf16 pairs and
+// stored over the first 64 TMEM columns of the tile (chunk c is written to
+// columns [16c, 16c + 16), all of which chunks <= c have already read).
+// Returns the fp32 sum of the P values.  Packed f32x2 FMA/ADD halve the ALU
+// instruction count; the exponentials go to the MUFU pipe.
+template <bool MASK>
+__device__ __forceinline__ float exp_pass(uint32_t tS, int lim, float sl2, float neg_m)
+{
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+    const float2 scale = make_float2(sl2, sl2), shift = make_float2(neg_m, neg_m);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t x[32];
+        tmem_ld32(tS + c * 32, x);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            float2 sv = make_float2(__uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1]));
+            if (MASK) {
+                const int col = c * 32 + 2 * e;
+                sv.x = col < lim ? sv.x : -INFINITY;
+                sv.y = col + 1 < lim ? sv.y : -INFINITY;
+            }
+            const float2 t = ffma2(sv, scale, shift);
+            const float2 pv = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+            if (e & 1)
+                acc1 = fadd2(acc1, pv);
+            else
+                acc0 = fadd2(acc0, pv);
+            pk[e] = pack_bf16x2(pv.x, pv.y);
+        }
+        tmem_st16(tS + c * 16, pk);
+    }
+    const float2 acc = fadd2(acc0, acc1);
+    return acc.x + acc.y;
 }
 
 template <int D>
@@ -405,21 +472,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
                 }
                 tc_fence_after();
                 const int lim = ra_key_limit(w.cls, a, p.L) - w.tb * RA_TILE;
-                // pass 1: masked row max of the 128 scores
-                float mx = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t x[32];
-                    tmem_ld32(tS + c * 32, x);
-                    tmem_wait_ld();
-                    float m0 = -INFINITY, m1 = -INFINITY;
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        m0 = fmaxf(m0, c * 32 + e < lim ? __uint_as_float(x[e]) : -INFINITY);
-                        m1 = fmaxf(m1, c * 32 + e + 1 < lim ? __uint_as_float(x[e + 1]) : -INFINITY);
-                    }
-                    mx = fmaxf(mx, fmaxf(m0, m1));
-                }
+                // pass 1: row max of the 128 scores (masked only where some
+                // column of the warp's rows lies past its visibility bound)
+                const bool masked = !__all_sync(0xffffffffu, lim >= RA_TILE);
+                const float mx = masked ? row_max<true>(tS, lim) : row_max<false>(tS, lim);
                 const float m_tile = mx * sl2;  // -inf stays -inf
                 const bool resc = m_tile > m_run + LAZY_RESCALE_LOG2;
                 float alpha = 1.f;
@@ -443,26 +499,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
                 // pass 2: P = exp2(s log2e / sqrt(d) - m) as bf16 pairs over
                 // the first 64 columns (chunk c lands on columns already read)
                 const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-                float l0 = 0.f, l1 = 0.f;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t x[32];
-                    tmem_ld32(tS + c * 32, x);
-                    tmem_wait_ld();
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float s0 = c * 32 + 2 * e < lim ? __uint_as_float(x[2 * e]) : -INFINITY;
-                        const float s1 = c * 32 + 2 * e + 1 < lim ? __uint_as_float(x[2 * e + 1]) : -INFINITY;
-                        const float p0 = ex2_approx(fmaf(s0, sl2, neg_m));
-                        const float p1 = ex2_approx(fmaf(s1, sl2, neg_m));
-                        l0 += p0;
-                        l1 += p1;
-                        pk[e] = pack_bf16x2(p0, p1);
-                    }
-                    tmem_st16(tS + c * 16, pk);
-                }
-                l_run += l0 + l1;
+                l_run += masked ? exp_pass<true>(tS, lim, sl2, neg_m)
+                                : exp_pass<false>(tS, lim, sl2, neg_m);
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(bar(ctrl->p_full[t]));
@@ -597,6 +635,25 @@ cudaError_t launch_attn_tc(const TcLaunch &a, cudaStream_t st)
     if (a.d == 64)
         return launch_d<64>(a, st);
     return cudaErrorInvalidValue;
+}
+
+// The failure path under test: the same bounded wait, on an mbarrier that no
+// thread or copy ever arrives at.
+__global__ void ra_wait_probe_kernel(unsigned long long timeout_ns)
+{
+    __shared__ uint64_t bar;
+    __shared__ int abort;
+    const uint32_t b = smem_u32(&bar);
+    mbar_init(b, 1);
+    abort = 0;
+    fence_mbar_init();
+    mbar_wait(b, 0, &abort, timeout_ns, &g_ra_status, SITE_PROBE);
+}
+
+cudaError_t launch_wait_probe(unsigned long long timeout_ns, cudaStream_t st)
+{
+    ra_wait_probe_kernel<<<1, 1, 0, st>>>(timeout_ns);
+    return cudaGetLastError();
 }
 
 cudaError_t read_and_clear_device_status(unsigned int *status)

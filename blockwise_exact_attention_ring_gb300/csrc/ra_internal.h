@@ -50,4 +50,7 @@ cudaError_t launch_attn_tc(const TcLaunch &a, cudaStream_t st);
 // Device-side error word helpers (defined in ra_attn_sm103.cu).
 cudaError_t read_and_clear_device_status(unsigned int *status);
 
+// One-thread kernel whose bounded wait on a never-completed mbarrier runs out.
+cudaError_t launch_wait_probe(unsigned long long timeout_ns, cudaStream_t st);
+
 }  // namespace ra

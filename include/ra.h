@@ -225,6 +225,29 @@ ra_status ra_check(ra_stream_t stream);
 /* Human-readable name of a ra_status value; never NULL. */
 const char *ra_status_string(int status);
 
+/*
+ * ra_set_wait_timeout_ns - bound, in nanoseconds of the GPU's global timer,
+ * on every mbarrier wait inside the tensor-core kernel launched after this
+ * call (0 restores the default of 4 s).  A wait that runs out records
+ * RA_ERR_TIMEOUT in the device error word, the kernel drains its in-flight
+ * copies and MMAs, frees tensor memory and returns; ra_check() reports it.
+ * Source: the "Context Parallelism" page of freenetmedia.pl, section "Typowe
+ * bledy i pulapki": synchronisation mistakes give wrong results or hangs; here
+ * a broken handshake turns into an error status instead of a hang.
+ */
+void ra_set_wait_timeout_ns(unsigned long long timeout_ns);
+
+/*
+ * ra_wait_probe - launch a one-thread kernel that waits, with the same
+ * bounded wait the tensor-core kernel uses, on an mbarrier that nothing ever
+ * arrives at, for at most timeout_ns (1 ms .. 10 s).  The wait runs out, the
+ * kernel records RA_ERR_TIMEOUT in the device error word and returns, and the
+ * next ra_check() reports RA_ERR_TIMEOUT; the context stays usable.  Exists to
+ * test the failure path without faulting or hanging a GPU.
+ * RA_ERR_INVALID_ARG for a timeout outside the range.  Same source as above.
+ */
+ra_status ra_wait_probe(unsigned long long timeout_ns, ra_stream_t stream);
+
 /* Number of CUDA kernels this library has launched in the process so far
  * (all entry points, all devices).  Lets a caller count the launches inside
  * a timed region. */

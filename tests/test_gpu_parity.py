@@ -46,8 +46,8 @@ def _check(out, lse, q, k, v, causal, rows=None):
 
 # ---------------------------------------------------------------- fp32 path
 
-@pytest.mark.parametrize("layout,mode", itertools.product(["contiguous", "striped"],
-                                                           ["fused", "per_step"]))
+@pytest.mark.parametrize("layout,mode", list(itertools.product(["contiguous", "striped"],
+                                                                ["fused", "per_step"])))
 def test_page_example_fp32(layout, mode):
     """The pages' 4-device, block-8, dim-16 simulation on the seed-0 inputs."""
     q, k, v = _dev(*inputs.page_example_qkv())
