@@ -65,6 +65,8 @@ def lib():
     L.ra_wait_probe.argtypes = [ctypes.c_ulonglong, vp]
     L.ra_wait_probe.restype = i
     L.ra_launch_count.restype = ctypes.c_ulonglong
+    L.ra_schedule_units.argtypes = [i] * 9 + [vp, ll]
+    L.ra_schedule_units.restype = ll
     L.ra_schedule_stats.argtypes = [i, i, i, i, vp, vp]
     L.ra_schedule_stats.restype = ll
     for fn in ("ra_forward", "ra_forward_f32", "ra_forward_noalloc", "ra_forward_ws", "ra_permute",
@@ -200,3 +202,18 @@ def schedule_stats(layout: str, causal: bool, n_blocks: int, L: int):
     if total < 0:
         raise ValueError("invalid schedule request")
     return int(total), pairs, tiles
+
+
+def schedule_units(B, H, Hkv, S, n_blocks, layout="contiguous", causal=False, steps=None):
+    """Work units of the tensor-core kernel in dealing order: int array [n, 8]
+    of (bh0, ta0, bh1, ta1, rank, cost, tile1_valid, 0).  steps: None for the
+    whole ring, or a single step index."""
+    s0, s1 = (0, n_blocks) if steps is None else (steps, steps + 1)
+    L = lib()
+    n = L.ra_schedule_units(B, H, Hkv, S, n_blocks, LAYOUTS[layout], int(bool(causal)), s0, s1, None, 0)
+    if n < 0:
+        raise ValueError("invalid schedule request")
+    out = np.zeros((n, 8), dtype=np.int32)
+    L.ra_schedule_units(B, H, Hkv, S, n_blocks, LAYOUTS[layout], int(bool(causal)), s0, s1,
+                        out.ctypes.data, n)
+    return out

@@ -6,9 +6,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
-#include <map>
 #include <mutex>
-#include <tuple>
 #include <vector>
 
 #include <cuda_runtime.h>
@@ -122,93 +120,6 @@ WsLayout ws_layout(const Problem &p)
     return w;
 }
 
-// ------------------------------------------------------------------ scheduler
-// Units for the tensor-core kernel: pairs of 128-row query tiles sharing a kv
-// head, cost = key tiles visited over ring steps [s_begin, s_end), sorted
-// heaviest first (stable), units that visit nothing dropped.
-std::vector<RaUnit> build_units(int B, int H, int Hkv, int S, int N, int layout, int causal,
-                                int s_begin, int s_end)
-{
-    const int L = S / N;
-    const int ntiles = (L + RA_TILE - 1) / RA_TILE;
-    const int group = H / Hkv;
-    std::vector<RaUnit> units;
-    auto cost_of = [&](int i, int ta_max) {
-        int c = 0;
-        for (int s = s_begin; s < s_end; ++s)
-            c += ra_kv_tiles(ra_block_class(layout, causal, i, ra_ring_block(i, s, N)), ta_max, ntiles);
-        return c;
-    };
-    auto push = [&](int bh0, int ta0, int bh1, int ta1, int i, bool valid1) {
-        RaUnit u{};
-        u.bh0 = bh0, u.ta0 = ta0, u.bh1 = bh1, u.ta1 = ta1, u.rank = i;
-        u.tile1_valid = valid1 ? 1 : 0;
-        u.cost = cost_of(i, std::max(ta0, ta1));
-        if (u.cost > 0)
-            units.push_back(u);
-    };
-    if (group % 2 == 0) {
-        // two query heads of one kv group, same positions: identical masks
-        for (int b = 0; b < B; ++b)
-            for (int h = 0; h < H; h += 2)
-                for (int i = 0; i < N; ++i)
-                    for (int ta = 0; ta < ntiles; ++ta)
-                        push(b * H + h, ta, b * H + h + 1, ta, i, true);
-    } else {
-        // two adjacent query tiles of one head
-        for (int b = 0; b < B; ++b)
-            for (int h = 0; h < H; ++h)
-                for (int i = 0; i < N; ++i)
-                    for (int ta = 0; ta < ntiles; ta += 2) {
-                        const bool has1 = ta + 1 < ntiles;
-                        push(b * H + h, ta, b * H + h, has1 ? ta + 1 : ta, i, has1);
-                    }
-    }
-    std::stable_sort(units.begin(), units.end(),
-                     [](const RaUnit &x, const RaUnit &y) { return x.cost > y.cost; });
-    return units;
-}
-
-struct DeviceUnits {
-    RaUnit *ptr = nullptr;
-    int count = 0;
-};
-
-std::mutex g_sched_mu;
-std::map<std::tuple<int, int, int, int, int, int, int, int, int, int>, DeviceUnits> g_sched;
-
-// Device copy of the unit list, built once per (device, problem, step range)
-// and kept for the life of the process.
-ra_status get_units(int B, int H, int Hkv, int S, int N, int layout, int causal, int s_begin,
-                    int s_end, DeviceUnits *out)
-{
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
-        return RA_ERR_CUDA;
-    const auto key = std::make_tuple(dev, B, H, Hkv, S, N, layout, causal, s_begin, s_end);
-    std::lock_guard<std::mutex> lock(g_sched_mu);
-    auto it = g_sched.find(key);
-    if (it != g_sched.end()) {
-        *out = it->second;
-        return RA_OK;
-    }
-    std::vector<RaUnit> units = build_units(B, H, Hkv, S, N, layout, causal, s_begin, s_end);
-    DeviceUnits du;
-    du.count = (int)units.size();
-    if (!units.empty()) {
-        if (cudaMalloc(&du.ptr, units.size() * sizeof(RaUnit)) != cudaSuccess)
-            return RA_ERR_NO_MEMORY;
-        if (cudaMemcpy(du.ptr, units.data(), units.size() * sizeof(RaUnit), cudaMemcpyHostToDevice) !=
-            cudaSuccess) {
-            cudaFree(du.ptr);
-            return RA_ERR_CUDA;
-        }
-    }
-    g_sched[key] = du;
-    *out = du;
-    return RA_OK;
-}
-
 // ------------------------------------------------------------------ forward
 ra_status attention_pass(const Problem &p, const void *q, const void *k, const void *v, void *out,
                          float *lse, int s_begin, int s_end, bool out_f32, int sm, cudaStream_t st)
@@ -219,19 +130,14 @@ ra_status attention_pass(const Problem &p, const void *q, const void *k, const v
         count_launch();
         return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
     }
-    DeviceUnits du;
-    ra_status rs = get_units(p.B, p.H, p.Hkv, p.S, p.N, p.layout, p.causal, s_begin, s_end, &du);
-    if (rs != RA_OK)
-        return rs;
     ra::TcLaunch a{};
     a.q = q, a.k = k, a.v = v, a.out = out, a.lse = lse;
-    a.units = du.ptr, a.n_units = du.count;
     a.B = p.B, a.H = p.H, a.Hkv = p.Hkv, a.S = p.S, a.d = p.d, a.N = p.N;
     a.layout = p.layout, a.causal = p.causal, a.s_begin = s_begin, a.s_end = s_end;
     a.out_f32 = out_f32 ? 1 : 0;
     a.timeout_ns = g_timeout_ns;
     a.sm_count = sm;
-    if (a.n_units > 0)
+    if (ra_unit_count(ra_unit_space(p.B, p.H, p.Hkv, p.S, p.N, p.layout, p.causal, s_begin, s_end)) > 0)
         count_launch();
     return ra::launch_attn_tc(a, st) == cudaSuccess ? RA_OK : RA_ERR_CUDA;
 }
@@ -461,6 +367,24 @@ const char *ra_status_string(int status)
 
 const char *ra_version(void) { return "ra 0.1.0 sm_103a"; }
 
+long long ra_schedule_units(int B, int H, int Hkv, int S, int n_blocks, int layout, int causal,
+                            int s_begin, int s_end, int *units, long long capacity)
+{
+    const Problem p{B, H, Hkv, S, 64, n_blocks, layout, causal, RA_DTYPE_BF16, RA_MODE_FUSED};
+    if (check_problem(p) != RA_OK || s_begin < 0 || s_end > n_blocks || s_begin >= s_end ||
+        (!(s_begin == 0 && s_end == n_blocks) && s_end != s_begin + 1))
+        return -1;
+    const RaUnitSpace sp = ra_unit_space(B, H, Hkv, S, n_blocks, layout, causal, s_begin, s_end);
+    const long long n = ra_unit_count(sp);
+    for (long long u = 0; units && u < n && u < capacity; ++u) {
+        const RaUnit U = ra_unit_decode(sp, u);
+        int *o = units + 8 * u;
+        o[0] = U.bh0, o[1] = U.ta0, o[2] = U.bh1, o[3] = U.ta1;
+        o[4] = U.rank, o[5] = U.cost, o[6] = U.tile1_valid, o[7] = 0;
+    }
+    return n;
+}
+
 long long ra_schedule_stats(int layout, int causal, int n_blocks, int L, long long *pairs, long long *tiles)
 {
     if (n_blocks < 1 || L < 1 || (layout != 0 && layout != 1) || (causal != 0 && causal != 1))
@@ -540,24 +464,22 @@ extern "C" ra_status ra_forward_noalloc(const void *q, const void *k, const void
     if (overlaps(out, qb, lse, lb))
         return RA_ERR_INVALID_ARG;
 
-    // scratch: [work list][striped q', k', v', out', lse'], 256-byte aligned
-    const std::vector<RaUnit> units = build_units(B, H, Hkv, S, n_blocks, layout, causal, 0, n_blocks);
+    // scratch (striped only): [q', k', v', out', lse'], 256-byte aligned
     const bool striped = layout == RA_LAYOUT_STRIPED;
-    const size_t units_bytes = align256(units.size() * sizeof(RaUnit));
-    const size_t off_q = units_bytes, off_k = off_q + align256(qb), off_v = off_k + align256(kvb);
+    const size_t off_q = 0, off_k = off_q + align256(qb), off_v = off_k + align256(kvb);
     const size_t off_o = off_v + align256(kvb), off_l = off_o + align256(qb);
-    const size_t need = striped ? off_l + align256(lb) : units_bytes;
+    const size_t need = striped ? off_l + align256(lb) : 0;
     if (need > RA_NOALLOC_SCRATCH_BYTES)
         return RA_ERR_SCRATCH_LIMIT;
 
-    void *scratch = nullptr;
-    if ((rs = noalloc_scratch(&scratch)) != RA_OK)
-        return rs;
-    char *base = static_cast<char *>(scratch);
+    char *base = nullptr;
+    if (striped) {
+        void *scratch = nullptr;
+        if ((rs = noalloc_scratch(&scratch)) != RA_OK)
+            return rs;
+        base = static_cast<char *>(scratch);
+    }
     cudaStream_t st = (cudaStream_t)stream;
-    if (!units.empty() && cudaMemcpyAsync(base, units.data(), units.size() * sizeof(RaUnit),
-                                          cudaMemcpyHostToDevice, st) != cudaSuccess)
-        return RA_ERR_CUDA;
 
     const int sm = sm_count_current();
     const long long row_bytes = (long long)d * 2;
@@ -577,14 +499,12 @@ extern "C" ra_status ra_forward_noalloc(const void *q, const void *k, const void
     }
     ra::TcLaunch a{};
     a.q = qk, a.k = kk, a.v = vk, a.out = ok_out, a.lse = ok_lse;
-    a.units = reinterpret_cast<const RaUnit *>(base), a.n_units = (int)units.size();
     a.B = B, a.H = H, a.Hkv = Hkv, a.S = S, a.d = d, a.N = n_blocks;
     a.layout = layout, a.causal = causal, a.s_begin = 0, a.s_end = n_blocks;
     a.out_f32 = 0;
     a.timeout_ns = g_timeout_ns;
     a.sm_count = sm;
-    if (a.n_units > 0)
-        count_launch();
+    count_launch();
     if (ra::launch_attn_tc(a, st) != cudaSuccess)
         return RA_ERR_CUDA;
     if (striped) {

@@ -18,10 +18,11 @@
 //   * warp 0 issues TMA loads (Q once per unit, K and V per 128-key tile, in
 //     128-byte swizzled 64-column slabs), warp 1 issues tcgen05.mma,
 //     warps 4-7 and 8-11 run the online softmax for query tile 0 and 1;
-//   * S = Q K^T goes to TMEM (fp32, 128 lanes x 128 columns per tile); the
-//     softmax warps read a row per thread, write P = exp2(S log2e/sqrt(d) - m)
-//     back over the same columns as packed bf16, and O += P V reads P from
-//     TMEM as the A operand and V from shared memory (MN-major);
+//   * S = Q K^T goes to TMEM (fp32, 128 lanes x 128 columns per tile); each
+//     softmax thread reads its row once (two 64-column loads, one wait),
+//     writes P = exp2(S log2e/sqrt(d) - m) back over the same columns as
+//     packed bf16, and O += P V reads P from TMEM as the A operand and V from
+//     shared memory (MN-major);
 //   * the running max is rescaled lazily: O and l are only corrected when a
 //     row's max grows by more than 2^8, which the final division makes exact;
 //   * every mbarrier wait is bounded; a wait that runs out records an error
@@ -45,7 +46,7 @@ __device__ unsigned int g_ra_status = 0;
 
 namespace {
 
-constexpr int NUM_THREADS = 384;
+constexpr int NUM_THREADS = 384;  // 12 warps: TMA, MMA, 2 spare, 2 x 4 softmax
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float LAZY_RESCALE_LOG2 = 8.0f;
 constexpr float LN2 = 0.693147180559945309f;
@@ -81,7 +82,7 @@ static_assert(sizeof(Ctrl) <= 256, "control block");
 
 struct TcParams {
     CUtensorMap tm_q, tm_k, tm_v;
-    const RaUnit *units;
+    RaUnitSpace sp;  // the launch's work units, decoded on the fly
     void *out;
     float *lse;
     int n_units, H, Hkv, S, L, N, layout, causal, s_begin, s_end, out_f32, ntiles;
@@ -120,7 +121,7 @@ struct KvWalk {
     }
 };
 
-// Units are dealt to CTAs in snake order over the cost-sorted list.
+// Units are dealt to CTAs in snake order over the heaviest-first enumeration.
 __device__ __forceinline__ int unit_index(int round, int cta, int G)
 {
     return round * G + ((round & 1) ? (G - 1 - cta) : cta);
@@ -155,82 +156,79 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap *tm, i
         tma_load_2d(dst + h * Cfg<D>::SLAB, tm, h * 64, row, bar, pol);
 }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
+// One online-softmax step for the query row this thread owns.  The row's 128
+// scores of the current key tile are read from TMEM once (two 64-column
+// loads, one wait); columns at or past `lim` count as -inf when MASK.  The
+// running max m (log2 domain, scores scaled by sl2 = log2e / sqrt(d)) only
+// moves when the tile max exceeds it by more than 2^8, and then O (in TMEM,
+// when has_o) and l are rescaled by 2^(m_old - m_new); the final division
+// cancels the common factor, so the result is exact.  P = 2^(s sl2 - m) is
+// packed to bf16 pairs over the first 64 columns of the tile (all scores are
+// in registers by then) for the P V MMA, and l accumulates the fp32 P.
+template <int D, bool MASK>
+__device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, int lim, float sl2, bool has_o,
+                                             float &m_run, float &l_run)
 {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
-        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
-          "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
-          "r"(r[13]), "r"(r[14]), "r"(r[15])
-        : "memory");
-}
-
-// Row max of one thread's 128 scores in TMEM (4 loads of 32 columns), with
-// columns at or past `lim` treated as -inf when MASK.  Two max3 chains.
-template <bool MASK>
-__device__ __forceinline__ float row_max(uint32_t tS, int lim)
-{
+    const uint32_t ninf = __float_as_uint(-INFINITY);
     float ma = -INFINITY, mb = -INFINITY;
+    uint32_t xa[64], xb[64];
+    tmem_ld64(tS, xa);
+    tmem_ld64(tS + 64, xb);
+    tmem_wait_ld();
+    if (MASK) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        uint32_t x[32];
-        tmem_ld32(tS + c * 32, x);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-            float v0 = __uint_as_float(x[e]), v1 = __uint_as_float(x[e + 1]);
-            float v2 = __uint_as_float(x[e + 2]), v3 = __uint_as_float(x[e + 3]);
-            if (MASK) {
-                const int col = c * 32 + e;
-                v0 = col < lim ? v0 : -INFINITY;
-                v1 = col + 1 < lim ? v1 : -INFINITY;
-                v2 = col + 2 < lim ? v2 : -INFINITY;
-                v3 = col + 3 < lim ? v3 : -INFINITY;
-            }
-            ma = max3f(ma, v0, v1);
-            mb = max3f(mb, v2, v3);
+        for (int e = 0; e < 64; ++e) {
+            xa[e] = e < lim ? xa[e] : ninf;
+            xb[e] = e + 64 < lim ? xb[e] : ninf;
         }
     }
-    return fmaxf(ma, mb);
-}
-
-// P = exp2(s * sl2 + neg_m) for the 128 scores, packed to bf16 pairs and
-// stored over the first 64 TMEM columns of the tile (chunk c is written to
-// columns [16c, 16c + 16), all of which chunks <= c have already read).
-// Returns the fp32 sum of the P values.  Packed f32x2 FMA/ADD halve the ALU
-// instruction count; the exponentials go to the MUFU pipe.
-template <bool MASK>
-__device__ __forceinline__ float exp_pass(uint32_t tS, int lim, float sl2, float neg_m)
-{
-    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int e = 0; e < 64; e += 2) {
+        ma = max3f(ma, __uint_as_float(xa[e]), __uint_as_float(xa[e + 1]));
+        mb = max3f(mb, __uint_as_float(xb[e]), __uint_as_float(xb[e + 1]));
+    }
+    const float m_tile = fmaxf(ma, mb) * sl2;  // -inf stays -inf
+    const bool resc = m_tile > m_run + LAZY_RESCALE_LOG2;
+    float alpha = 1.f;
+    if (resc) {
+        alpha = ex2_approx(m_run - m_tile);  // 0 when m_run = -inf
+        m_run = m_tile;
+        l_run *= alpha;
+    }
+    const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
     const float2 scale = make_float2(sl2, sl2), shift = make_float2(neg_m, neg_m);
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        uint32_t x[32];
-        tmem_ld32(tS + c * 32, x);
-        tmem_wait_ld();
-        uint32_t pk[16];
+    for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            float2 sv = make_float2(__uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1]));
-            if (MASK) {
-                const int col = c * 32 + 2 * e;
-                sv.x = col < lim ? sv.x : -INFINITY;
-                sv.y = col + 1 < lim ? sv.y : -INFINITY;
-            }
-            const float2 t = ffma2(sv, scale, shift);
-            const float2 pv = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+        for (int e = 0; e < 32; ++e) {
+            const uint32_t u0 = h ? xb[2 * e] : xa[2 * e];
+            const uint32_t u1 = h ? xb[2 * e + 1] : xa[2 * e + 1];
+            const float2 t2 = ffma2(make_float2(__uint_as_float(u0), __uint_as_float(u1)), scale, shift);
+            const float2 pv = make_float2(ex2_approx(t2.x), ex2_approx(t2.y));
             if (e & 1)
                 acc1 = fadd2(acc1, pv);
             else
                 acc0 = fadd2(acc0, pv);
             pk[e] = pack_bf16x2(pv.x, pv.y);
         }
-        tmem_st16(tS + c * 16, pk);
+        tmem_st32(tS + h * 32, pk);
     }
     const float2 acc = fadd2(acc0, acc1);
-    return acc.x + acc.y;
+    l_run += acc.x + acc.y;
+    if (has_o && __any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tO + c * 32, o);
+        }
+    }
 }
 
 template <int D>
@@ -297,7 +295,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
                 const int u = unit_index(r, blockIdx.x, gridDim.x);
                 if (u >= p.n_units)
                     break;
-                const RaUnit U = p.units[u];
+                const RaUnit U = ra_unit_decode(p.sp, u);
                 if (qcnt > 0 && !(ok = wait1(bar(ctrl->q_empty), (qcnt - 1) & 1, abort, tmo,
                                                  SITE_Q_EMPTY)))
                     break;
@@ -373,7 +371,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
                 const int u = unit_index(r, blockIdx.x, gridDim.x);
                 if (u >= p.n_units)
                     break;
-                const int n = p.units[u].cost;
+                const int n = ra_unit_decode(p.sp, u).cost;
                 if (!(ok = wait1(bar(ctrl->q_full), qcnt & 1, abort, tmo, SITE_Q_FULL)))
                     break;
                 int ks = kcnt % C::KSTAGES;
@@ -453,7 +451,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
             const int u = unit_index(rr, blockIdx.x, gridDim.x);
             if (u >= p.n_units)
                 break;
-            const RaUnit U = p.units[u];
+            const RaUnit U = ra_unit_decode(p.sp, u);
             const int bh = t ? U.bh1 : U.bh0;
             const int ta = t ? U.ta1 : U.ta0;
             const bool store = (t == 0) || U.tile1_valid;
@@ -472,35 +470,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
                 }
                 tc_fence_after();
                 const int lim = ra_key_limit(w.cls, a, p.L) - w.tb * RA_TILE;
-                // pass 1: row max of the 128 scores (masked only where some
-                // column of the warp's rows lies past its visibility bound)
+                // masked only where some column of the warp's rows lies past
+                // its visibility bound (diagonal and ragged tiles)
                 const bool masked = !__all_sync(0xffffffffu, lim >= RA_TILE);
-                const float mx = masked ? row_max<true>(tS, lim) : row_max<false>(tS, lim);
-                const float m_tile = mx * sl2;  // -inf stays -inf
-                const bool resc = m_tile > m_run + LAZY_RESCALE_LOG2;
-                float alpha = 1.f;
-                if (resc) {
-                    alpha = ex2_approx(m_run - m_tile);  // 0 when m_run = -inf
-                    m_run = m_tile;
-                    l_run *= alpha;
-                }
-                if (jj > 0 && __any_sync(0xffffffffu, resc)) {
-#pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t o[32];
-                        tmem_ld32(tO + c * 32, o);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32(tO + c * 32, o);
-                    }
-                }
-                // pass 2: P = exp2(s log2e / sqrt(d) - m) as bf16 pairs over
-                // the first 64 columns (chunk c lands on columns already read)
-                const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-                l_run += masked ? exp_pass<true>(tS, lim, sl2, neg_m)
-                                : exp_pass<false>(tS, lim, sl2, neg_m);
+                if (masked)
+                    softmax_step<D, true>(tS, tO, lim, sl2, jj > 0, m_run, l_run);
+                else
+                    softmax_step<D, false>(tS, tO, lim, sl2, jj > 0, m_run, l_run);
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(bar(ctrl->p_full[t]));
@@ -609,19 +585,22 @@ cudaError_t launch_d(const TcLaunch &a, cudaStream_t st)
         !encode_rows(&p.tm_k, a.k, (long long)a.B * a.Hkv * a.S, D) ||
         !encode_rows(&p.tm_v, a.v, (long long)a.B * a.Hkv * a.S, D))
         return cudaErrorInvalidValue;
-    p.units = a.units;
+    p.sp = ra_unit_space(a.B, a.H, a.Hkv, a.S, a.N, a.layout, a.causal, a.s_begin, a.s_end);
+    const long long n_units = ra_unit_count(p.sp);
+    if (n_units > 0x7fffffffll)
+        return cudaErrorInvalidValue;
     p.out = a.out;
     p.lse = a.lse;
-    p.n_units = a.n_units;
+    p.n_units = (int)n_units;
     p.H = a.H, p.Hkv = a.Hkv, p.S = a.S, p.N = a.N, p.L = a.S / a.N;
     p.layout = a.layout, p.causal = a.causal;
     p.s_begin = a.s_begin, p.s_end = a.s_end, p.out_f32 = a.out_f32;
     p.ntiles = (p.L + RA_TILE - 1) / RA_TILE;
     p.scale_log2 = 1.4426950408889634f / sqrtf((float)D);
     p.timeout_ns = a.timeout_ns;
-    if (a.n_units <= 0)
+    if (p.n_units <= 0)
         return cudaSuccess;
-    const int grid = a.n_units < a.sm_count ? a.n_units : a.sm_count;
+    const int grid = p.n_units < a.sm_count ? p.n_units : a.sm_count;
     ra_attn_tc_kernel<D><<<grid, NUM_THREADS, C::SMEM, st>>>(p);
     return cudaGetLastError();
 }

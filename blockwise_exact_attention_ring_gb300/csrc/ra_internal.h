@@ -28,13 +28,12 @@ void launch_finalize(const float *run, const float *run_lse, void *out, float *l
                      long long rows_total, int S, int N, int striped, int d, int sm_count,
                      cudaStream_t st);
 
-// Tensor-core attention over a device list of units (see RaUnit).
+// Tensor-core attention; the work units (see RaUnitSpace) are enumerated in
+// the kernel, so the launch needs no device-side list.
 struct TcLaunch {
     const void *q, *k, *v;       // bf16, kernel (possibly striped) order
     void *out;                   // bf16 (out_f32 = 0) or fp32 normalised partial
     float *lse;
-    const RaUnit *units;
-    int n_units;
     int B, H, Hkv, S, d, N;
     int layout, causal;
     int s_begin, s_end;          // ring steps walked by every unit

@@ -84,3 +84,88 @@ struct RaUnit {
     int tile1_valid;
     int pad;
 };
+
+// Key tiles a unit of rank i visits over ring steps [s_begin, s_end).
+RA_HD int ra_unit_cost(int layout, int causal, int i, int ta_max, int ntiles, int n_blocks,
+                       int s_begin, int s_end)
+{
+    int c = 0;
+    for (int s = s_begin; s < s_end; ++s)
+        c += ra_kv_tiles(ra_block_class(layout, causal, i, ra_ring_block(i, s, n_blocks)), ta_max,
+                         ntiles);
+    return c;
+}
+
+// The units of one launch, enumerated heaviest first without any stored list.
+// A unit is (column x, rank i, tile slot y): x runs over pairs of query heads
+// of one kv group (group size even: both heads share positions and masks) or
+// over single heads (odd group: the unit takes tiles 2y and 2y + 1 of one
+// head).  Ranks [i_lo, N) are active: all of them, except that at a single
+// contiguous causal ring step s only ranks i >= s hold a visible block.
+// Order: x fastest; then, when the cost grows with the rank (contiguous
+// causal over all steps: cost = i ntiles + tiles of the diagonal block),
+// rank descending then tile descending, otherwise tile descending then rank
+// descending (the cost depends on the tile only, or on nothing).
+struct RaUnitSpace {
+    int X, Y;          // columns, tile slots per rank
+    int i_lo, n_act;   // active ranks [i_lo, i_lo + n_act)
+    int ntiles;        // 128-row tiles per rank block
+    int head_pairs;    // 1: two heads per unit; 0: two tiles of one head
+    int rank_outer;    // 1: rank-major order; 0: tile-major order
+    int H, N, layout, causal, s_begin, s_end;
+};
+
+RA_HD RaUnitSpace ra_unit_space(int B, int H, int Hkv, int S, int n_blocks, int layout, int causal,
+                                int s_begin, int s_end)
+{
+    RaUnitSpace sp;
+    const int L = S / n_blocks;
+    sp.ntiles = (L + RA_TILE - 1) / RA_TILE;
+    sp.head_pairs = ((H / Hkv) % 2 == 0) ? 1 : 0;
+    sp.X = sp.head_pairs ? B * H / 2 : B * H;
+    sp.Y = sp.head_pairs ? sp.ntiles : (sp.ntiles + 1) / 2;
+    const bool all_steps = s_begin == 0 && s_end == n_blocks;
+    sp.i_lo = (causal && layout == 0 && !all_steps) ? s_begin : 0;
+    sp.n_act = n_blocks - sp.i_lo;
+    sp.rank_outer = (causal && layout == 0 && all_steps) ? 1 : 0;
+    sp.H = H, sp.N = n_blocks, sp.layout = layout, sp.causal = causal;
+    sp.s_begin = s_begin, sp.s_end = s_end;
+    return sp;
+}
+
+RA_HD long long ra_unit_count(const RaUnitSpace &sp)
+{
+    return (long long)sp.X * sp.n_act * sp.Y;
+}
+
+RA_HD RaUnit ra_unit_decode(const RaUnitSpace &sp, long long u)
+{
+    const int x = (int)(u % sp.X);
+    const long long r = u / sp.X;
+    int i, y;
+    if (sp.rank_outer) {
+        i = sp.N - 1 - (int)(r / sp.Y);
+        y = sp.Y - 1 - (int)(r % sp.Y);
+    } else {
+        y = sp.Y - 1 - (int)(r / sp.n_act);
+        i = sp.N - 1 - (int)(r % sp.n_act);
+    }
+    RaUnit U;
+    if (sp.head_pairs) {
+        const int half = sp.H / 2;
+        U.bh0 = (x / half) * sp.H + 2 * (x % half);
+        U.bh1 = U.bh0 + 1;
+        U.ta0 = U.ta1 = y;
+        U.tile1_valid = 1;
+    } else {
+        U.bh0 = U.bh1 = x;
+        U.ta0 = 2 * y;
+        U.tile1_valid = 2 * y + 1 < sp.ntiles ? 1 : 0;
+        U.ta1 = U.tile1_valid ? 2 * y + 1 : 2 * y;
+    }
+    U.rank = i;
+    U.cost = ra_unit_cost(sp.layout, sp.causal, i, U.ta0 > U.ta1 ? U.ta0 : U.ta1, sp.ntiles, sp.N,
+                          sp.s_begin, sp.s_end);
+    U.pad = 0;
+    return U;
+}

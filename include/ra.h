@@ -123,11 +123,8 @@ size_t ra_workspace_bytes(int B, int H, int Hkv, int S, int d, int n_blocks, int
  * at least ra_workspace_bytes(...)); no per-call allocation.  dtype selects the
  * tensor type (RA_DTYPE_BF16: q, k, v, out bf16; RA_DTYPE_F32: all fp32).
  * RA_ERR_WORKSPACE if ws is null, misaligned or too small.  Calls sharing one
- * workspace must be ordered on the GPU (same stream or events).
- * Every bf16 entry point keeps, per device and problem shape, the ring-step
- * schedule (the tensor-core kernel's work list) in device memory: the first
- * call for a shape builds it on the host and copies it with one cudaMalloc
- * and one synchronous cudaMemcpy; it lives until the process exits.
+ * workspace must be ordered on the GPU (same stream or events).  The ring
+ * schedule needs no memory: the kernel enumerates its work units itself.
  */
 ra_status ra_forward_ws(const void *q, const void *k, const void *v, void *out, float *lse,
                         int B, int H, int Hkv, int S, int d, int n_blocks, int layout,
@@ -161,28 +158,23 @@ ra_status ra_forward_rank_major(const void *q, const void *k, const void *v, voi
  * that reserves its whole budget at start-up and forbids allocation after
  * that), and latency-critical loops that must not meet an allocation-time
  * synchronisation or an out-of-memory failure half way through.  ra_forward
- * gets its scratch with cudaMallocAsync and keeps each problem shape's
- * schedule in memory it cudaMallocs once; this entry point does neither.
+ * gets its striped scratch with cudaMallocAsync; this entry point does not.
  *
- * Its scratch (the schedule's work list and, for RA_LAYOUT_STRIPED, the
- * striped copies of q, k, v, out and lse) lives in one fixed array of
- * RA_NOALLOC_SCRATCH_BYTES (64 MiB) that is part of the library's device
- * image: every GPU that loads the library holds it until the process exits.
- * A problem whose scratch would not fit returns RA_ERR_SCRATCH_LIMIT and
- * enqueues nothing; contiguous problems need only the work list (32 bytes per
- * pair of 128-row query tiles), striped ones also 2 (B H + 2 B Hkv) S d + 4 B H S
- * bytes.  Nothing in the array has to start at zero: every byte a call reads
- * was written earlier by the same call.
+ * Its scratch (for RA_LAYOUT_STRIPED, the striped copies of q, k, v, out and
+ * lse: 2 (B H + 2 B Hkv) S d + 4 B H S bytes; contiguous problems need none)
+ * lives in one fixed array of RA_NOALLOC_SCRATCH_BYTES (64 MiB) that is part
+ * of the library's device image: every GPU that loads the library holds it
+ * until the process exits.  A problem whose scratch would not fit returns
+ * RA_ERR_SCRATCH_LIMIT and enqueues nothing.  Nothing in the array has to
+ * start at zero: every byte a call reads was written earlier by the same call.
  *
  * All calls on a device share the one array and it keeps the last call's
  * contents, so calls that can overlap on the GPU (different streams without
  * ordering between them) race: order them on one stream or with events.
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  The work list is copied in with
- * cudaMemcpyAsync from pageable host memory, which the driver stages before
- * returning.  Calls no cudaMalloc, cudaMallocAsync, cudaFree or other
- * allocating routine.
+ * before any stream capture.  Calls no cudaMalloc, cudaMallocAsync, cudaFree
+ * or other allocating routine.
  */
 #define RA_NOALLOC_SCRATCH_BYTES (64ull << 20)
 ra_status ra_forward_noalloc(const void *q, const void *k, const void *v, void *out, float *lse,
@@ -266,6 +258,19 @@ const char *ra_version(void);
  */
 long long ra_schedule_stats(int layout, int causal, int n_blocks, int L,
                             long long *pairs, long long *tiles);
+
+/*
+ * ra_schedule_units - host-only view of the tensor-core kernel's work units
+ * for ring steps [s_begin, s_end) (all steps, or a single step), in the order
+ * the kernel deals them to CTAs (heaviest first).  Unit u is written to
+ * units[8u .. 8u + 7] as {bh0, ta0, bh1, ta1, rank, cost, tile1_valid, 0}: two
+ * 128-row query tiles (batch*H + head, tile index within the rank's block) of
+ * rank `rank` that share a kv head, and the number of 128-key tiles they visit.
+ * Writes at most `capacity` units (units may be NULL); returns the total
+ * count, or -1 on bad input.  Source: as for ra_schedule_stats.
+ */
+long long ra_schedule_units(int B, int H, int Hkv, int S, int n_blocks, int layout, int causal,
+                            int s_begin, int s_end, int *units, long long capacity);
 
 #ifdef __cplusplus
 }

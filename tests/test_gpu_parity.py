@@ -80,6 +80,9 @@ BF16_SHAPES = [
     (2, 8, 2, 1024, 128, 8),    # L = 128, one tile per rank
     (1, 2, 1, 32, 64, 4),       # L = 8: a block far smaller than a tile
     (1, 4, 4, 512, 64, 1),      # one rank: plain attention
+    (3, 6, 3, 260, 128, 4),     # odd batch, group 2, L = 65
+    (1, 2, 2, 4, 64, 4),        # L = 1: one token per rank
+    (1, 1, 1, 1, 128, 1),       # a single token
 ]
 
 

@@ -65,3 +65,55 @@ def test_striping_balances_causal_work():
     crit_c = pc.max(axis=0).sum()   # L^2/2 + (N - 1) L^2
     crit_s = ps.max(axis=0).sum()   # N L (L + 1) / 2
     assert abs(crit_c / crit_s - (N - 0.5) / (N / 2)) < 0.01
+
+
+def _brute_units(B, H, Hkv, S, N, layout, causal, steps):
+    """Every (query head, query tile, rank) the kernel must cover, with the key
+    tiles its ring steps visit, computed from the masks on natural positions."""
+    L = S // N
+    ntiles = -(-L // 128)
+    order = oracle.stripe_order(S, N) if layout == "striped" else np.arange(S)
+    pos = order.reshape(N, L)
+    ss = range(N) if steps is None else [steps]
+    need = {}
+    for i in range(N):
+        for ta in range(ntiles):
+            t = pos[i][ta * 128:(ta + 1) * 128]
+            tiles = 0
+            for s in ss:
+                j = (i - s) % N
+                for tb in range(ntiles):
+                    u = pos[j][tb * 128:(tb + 1) * 128]
+                    if not causal or (u[None, :] <= t[:, None]).any():
+                        tiles += 1
+            for bh in range(B * H):
+                need[(bh, ta, i)] = tiles
+    return need
+
+
+@pytest.mark.parametrize("B,H,Hkv,S,N", [(1, 4, 2, 1024, 4), (2, 3, 1, 1536, 3),
+                                         (1, 2, 2, 640, 5), (1, 8, 2, 256, 2)])
+@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("steps", [None, 0, 1])
+def test_kernel_units_cover_every_tile_once_heaviest_first(B, H, Hkv, S, N, layout, causal, steps):
+    units = ra.schedule_units(B, H, Hkv, S, N, layout, causal, steps)
+    need = _brute_units(B, H, Hkv, S, N, layout, causal, steps)
+    seen = {}
+    for bh0, ta0, bh1, ta1, rank, cost, valid1, _ in units:
+        for bh, ta, ok in ((bh0, ta0, True), (bh1, ta1, bool(valid1))):
+            if not ok:
+                continue
+            key = (int(bh), int(ta), int(rank))
+            assert key not in seen, "tile scheduled twice"
+            seen[key] = int(cost)
+            # both tiles of a unit read the same kv head
+        g = H // Hkv
+        assert (bh0 % H) // g == (bh1 % H) // g and bh0 // H == bh1 // H
+    # a tile pair visits the union of its tiles' key tiles: cost >= each tile's need
+    active = {k: v for k, v in need.items() if v > 0}
+    assert set(seen) == set(active)
+    for k, c in seen.items():
+        assert c >= active[k]
+    costs = units[:, 5]
+    assert np.all(costs > 0) and np.all(np.diff(costs) <= 0), "not heaviest first"
