@@ -105,28 +105,39 @@ void launch_attn_f32(const float *q, const float *k, const float *v, float *out,
 
 // ---------------------------------------------------------------- permute
 // Striped row p = r L + a holds natural token t = a N + r.  Each thread moves
-// one VEC-byte word; the grid walks destination rows, so writes are
-// contiguous and each source row is read whole.
-template <typename VEC>
+// VEC-byte words; the grid walks destination rows, so writes are contiguous
+// and each source row is read whole.  Every thread keeps UNROLL independent
+// loads in flight before it stores, which HBM needs to reach its bandwidth.
+template <typename VEC, int UNROLL>
 __global__ void ra_permute_kernel(const VEC *__restrict__ src, VEC *__restrict__ dst,
                                   long long n_rows_total, int S, int L, int N,
                                   int words_per_row, int inverse)
 {
     const long long n = n_rows_total * words_per_row;
-    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
-         idx += (long long)gridDim.x * blockDim.x) {
-        const long long row = idx / words_per_row;
-        const int w = (int)(idx - row * words_per_row);
-        const long long bh = row / S;
-        const int x = (int)(row - bh * S);
-        // forward: x is the striped row p, read natural t(p)
-        // inverse: x is the natural token t, read striped p(t)
-        int other;
-        if (!inverse)
-            other = (x % L) * N + x / L;
-        else
-            other = (x % N) * L + x / N;
-        dst[idx] = src[(bh * S + other) * words_per_row + w];
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long base = blockIdx.x * (long long)blockDim.x + threadIdx.x; base < n;
+         base += stride * UNROLL) {
+        VEC v[UNROLL];
+        long long at[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const long long idx = base + u * stride;
+            at[u] = idx;
+            if (idx < n) {
+                const long long row = idx / words_per_row;
+                const int w = (int)(idx - row * words_per_row);
+                const long long bh = row / S;
+                const int x = (int)(row - bh * S);
+                // forward: x is the striped row p, read natural t(p)
+                // inverse: x is the natural token t, read striped p(t)
+                const int other = !inverse ? (x % L) * N + x / L : (x % N) * L + x / N;
+                v[u] = src[(bh * S + other) * words_per_row + w];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u)
+            if (at[u] < n)
+                dst[at[u]] = v[u];
     }
 }
 
@@ -142,15 +153,15 @@ void launch_permute(const void *src, void *dst, long long rows_total, int S, int
     };
     if (row_bytes % 16 == 0) {
         const int wpr = (int)(row_bytes / 16);
-        ra_permute_kernel<uint4><<<grid_for(rows_total * wpr), threads, 0, st>>>(
+        ra_permute_kernel<uint4, 4><<<grid_for(rows_total * wpr), threads, 0, st>>>(
             (const uint4 *)src, (uint4 *)dst, rows_total, S, L, N, wpr, inverse);
     } else if (row_bytes % 4 == 0) {
         const int wpr = (int)(row_bytes / 4);
-        ra_permute_kernel<uint32_t><<<grid_for(rows_total * wpr), threads, 0, st>>>(
+        ra_permute_kernel<uint32_t, 4><<<grid_for(rows_total * wpr), threads, 0, st>>>(
             (const uint32_t *)src, (uint32_t *)dst, rows_total, S, L, N, wpr, inverse);
     } else {
         const int wpr = (int)row_bytes;
-        ra_permute_kernel<uint8_t><<<grid_for(rows_total * wpr), threads, 0, st>>>(
+        ra_permute_kernel<uint8_t, 4><<<grid_for(rows_total * wpr), threads, 0, st>>>(
             (const uint8_t *)src, (uint8_t *)dst, rows_total, S, L, N, wpr, inverse);
     }
 }
