@@ -54,6 +54,7 @@ def lib():
     L.ra_workspace_bytes.argtypes = [i] * 10
     L.ra_workspace_bytes.restype = sz
     L.ra_forward_ws.argtypes = [vp] * 5 + [i] * 10 + [vp, sz, vp]
+    L.ra_forward_rank_major.argtypes = [vp] * 5 + [i] * 10 + [vp, sz, vp]
     L.ra_permute.argtypes = [vp, vp] + [i] * 7 + [vp]
     L.ra_merge.argtypes = [vp] * 4 + [ll, i, vp]
     L.ra_check.argtypes = [vp]
@@ -69,8 +70,8 @@ def lib():
     L.ra_schedule_units.restype = ll
     L.ra_schedule_stats.argtypes = [i, i, i, i, vp, vp]
     L.ra_schedule_stats.restype = ll
-    for fn in ("ra_forward", "ra_forward_f32", "ra_forward_noalloc", "ra_forward_ws", "ra_permute",
-               "ra_merge", "ra_check"):
+    for fn in ("ra_forward", "ra_forward_f32", "ra_forward_noalloc", "ra_forward_ws",
+               "ra_forward_rank_major", "ra_permute", "ra_merge", "ra_check"):
         getattr(L, fn).restype = i
     _lib = L
     return L

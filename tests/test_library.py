@@ -89,3 +89,14 @@ def test_permute_and_merge_validation():
     assert L.ra_permute(Q, Q, 1, 1, 32, 8, 2, 4, 0, None) == rb.RA_ERR_INVALID_ARG   # in place
     assert L.ra_merge(Q, K, V, OUT, 10, 6, None) == rb.RA_ERR_INVALID_ARG           # d % 4
     assert L.ra_merge(Q, K, Q, OUT, 10, 8, None) == rb.RA_ERR_INVALID_ARG           # aliasing
+
+
+def test_every_declared_function_has_ctypes_signature():
+    """Sizes above 2^31 (workspaces, row counts) must not be truncated: every
+    entry point the header declares gets explicit argument types."""
+    L = ra.lib()
+    for n in rb.header_functions():
+        f = getattr(L, n)
+        if n in ("ra_version", "ra_launch_count"):
+            continue
+        assert f.argtypes is not None, n
