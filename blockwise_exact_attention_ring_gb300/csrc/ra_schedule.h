@@ -105,7 +105,8 @@ RA_HD int ra_unit_cost(int layout, int causal, int i, int ta_max, int ntiles, in
 // Order: x fastest; then, when the cost grows with the rank (contiguous
 // causal over all steps: cost = i ntiles + tiles of the diagonal block),
 // rank descending then tile descending, otherwise tile descending then rank
-// descending (the cost depends on the tile only, or on nothing).
+// descending (the cost depends on the tile only, or on nothing).  Large
+// problems put the kv head outermost (see RA_KV_OUTER_ROWS).
 struct RaUnitSpace {
     int X, Y;          // columns, tile slots per rank
     int i_lo, n_act;   // active ranks [i_lo, i_lo + n_act)
@@ -113,7 +114,15 @@ struct RaUnitSpace {
     int head_pairs;    // 1: two heads per unit; 0: two tiles of one head
     int rank_outer;    // 1: rank-major order; 0: tile-major order
     int H, N, layout, causal, s_begin, s_end;
+    int kv_heads;      // B * Hkv
+    int kv_outer;      // 1: kv head is the outermost index of the order
 };
+
+// Key/value rows (B * Hkv * S) from which the dealing order groups work by kv
+// head: below this the K and V of all heads stay in L2 and a global
+// heaviest-first order balances the tail better; above it (e.g. 256K tokens
+// x 8 kv heads = 1 GB of K and V) grouping by head keeps L2 reuse.
+#define RA_KV_OUTER_ROWS (1ll << 20)
 
 RA_HD RaUnitSpace ra_unit_space(int B, int H, int Hkv, int S, int n_blocks, int layout, int causal,
                                 int s_begin, int s_end)
@@ -130,6 +139,8 @@ RA_HD RaUnitSpace ra_unit_space(int B, int H, int Hkv, int S, int n_blocks, int 
     sp.rank_outer = (causal && layout == 0 && all_steps) ? 1 : 0;
     sp.H = H, sp.N = n_blocks, sp.layout = layout, sp.causal = causal;
     sp.s_begin = s_begin, sp.s_end = s_end;
+    sp.kv_heads = B * Hkv;
+    sp.kv_outer = (long long)B * Hkv * S >= RA_KV_OUTER_ROWS ? 1 : 0;
     return sp;
 }
 
@@ -140,8 +151,21 @@ RA_HD long long ra_unit_count(const RaUnitSpace &sp)
 
 RA_HD RaUnit ra_unit_decode(const RaUnitSpace &sp, long long u)
 {
-    const int x = (int)(u % sp.X);
-    const long long r = u / sp.X;
+    int x;
+    long long r;
+    if (sp.kv_outer) {
+        // kv head outermost: the CTAs in flight share one kv head's K and V
+        // instead of streaming every head's at once
+        const int Xg = sp.X / sp.kv_heads;  // columns per kv head
+        const long long per_kv = (long long)Xg * sp.n_act * sp.Y;
+        const int kvi = (int)(u / per_kv);
+        const long long rem = u - kvi * per_kv;
+        x = kvi * Xg + (int)(rem % Xg);
+        r = rem / Xg;
+    } else {
+        x = (int)(u % sp.X);
+        r = u / sp.X;
+    }
     int i, y;
     if (sp.rank_outer) {
         i = sp.N - 1 - (int)(r / sp.Y);

@@ -115,5 +115,33 @@ def test_kernel_units_cover_every_tile_once_heaviest_first(B, H, Hkv, S, N, layo
     assert set(seen) == set(active)
     for k, c in seen.items():
         assert c >= active[k]
+    _check_order(units, H, Hkv, B * Hkv * S >= (1 << 20))
+
+
+def _check_order(units, H, Hkv, kv_outer):
     costs = units[:, 5]
-    assert np.all(costs > 0) and np.all(np.diff(costs) <= 0), "not heaviest first"
+    assert np.all(costs > 0)
+    if not kv_outer:
+        assert np.all(np.diff(costs) <= 0), "not heaviest first"
+        return
+    # kv head outermost (the CTAs in flight share one head's K and V), and
+    # heaviest first within each kv head
+    g = H // Hkv
+    kvh = (units[:, 0] // H) * Hkv + (units[:, 0] % H) // g
+    assert np.all(np.diff(kvh) >= 0), "kv heads interleaved"
+    for h in np.unique(kvh):
+        c = costs[kvh == h]
+        assert np.all(np.diff(c) <= 0), "not heaviest first within a kv head"
+
+
+@pytest.mark.parametrize("layout,causal", [("contiguous", True), ("striped", True),
+                                           ("contiguous", False)])
+def test_large_problem_units_grouped_by_kv_head(layout, causal):
+    """256K tokens x 8 kv heads: every tile pair listed once, kv head outermost."""
+    B, H, Hkv, S, N = 1, 32, 8, 262144, 8
+    units = ra.schedule_units(B, H, Hkv, S, N, layout, causal)
+    L, ntiles = S // N, S // N // 128
+    assert len(units) == (B * H // 2) * N * ntiles
+    keys = set(map(tuple, units[:, [0, 1, 4]].tolist()))
+    assert len(keys) == len(units)
+    _check_order(units, H, Hkv, True)
