@@ -7,9 +7,9 @@ the library has not been built (``build.build()``).
 """
 from . import inputs  # noqa: F401
 from .binding import (RaError, check, forward, lib, merge, permute,  # noqa: F401
-                      schedule_stats, schedule_units, status_string, version,
-                      workspace_bytes)
+                      schedule_stats, schedule_units, set_kernel_variant, status_string,
+                      version, workspace_bytes)
 
 __all__ = ["inputs", "RaError", "check", "forward", "lib", "merge", "permute",
-           "schedule_stats", "schedule_units", "status_string", "version",
+           "schedule_stats", "schedule_units", "set_kernel_variant", "status_string", "version",
            "workspace_bytes"]

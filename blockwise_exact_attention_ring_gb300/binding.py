@@ -61,6 +61,8 @@ def lib():
     L.ra_status_string.argtypes = [i]
     L.ra_status_string.restype = ctypes.c_char_p
     L.ra_version.restype = ctypes.c_char_p
+    L.ra_set_kernel_variant.argtypes = [i]
+    L.ra_set_kernel_variant.restype = i
     L.ra_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
     L.ra_set_wait_timeout_ns.restype = None
     L.ra_wait_probe.argtypes = [ctypes.c_ulonglong, vp]
@@ -218,3 +220,12 @@ def schedule_units(B, H, Hkv, S, n_blocks, layout="contiguous", causal=False, st
     L.ra_schedule_units(B, H, Hkv, S, n_blocks, LAYOUTS[layout], int(bool(causal)), s0, s1,
                         out.ctypes.data, n)
     return out
+
+
+def set_kernel_variant(variant: int) -> int:
+    """0 automatic, 1 single-CTA, 2 CTA-pair tensor-core kernel; returns the
+    previous setting."""
+    prev = lib().ra_set_kernel_variant(int(variant))
+    if prev < 0:
+        raise ValueError(f"invalid kernel variant {variant}")
+    return prev

@@ -22,6 +22,7 @@ namespace {
 constexpr unsigned long long kDefaultTimeoutNs = 4000000000ull;  // 4 s per wait
 unsigned long long g_timeout_ns = kDefaultTimeoutNs;
 std::atomic<unsigned long long> g_launches{0};
+std::atomic<int> g_kernel_variant{0};  // 0 auto, 1 single-CTA, 2 CTA pair
 
 void count_launch(unsigned long long n = 1) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
@@ -139,7 +140,10 @@ ra_status attention_pass(const Problem &p, const void *q, const void *k, const v
     a.sm_count = sm;
     if (ra_unit_count(ra_unit_space(p.B, p.H, p.Hkv, p.S, p.N, p.layout, p.causal, s_begin, s_end)) > 0)
         count_launch();
-    return ra::launch_attn_tc(a, st) == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+    const int variant = g_kernel_variant.load(std::memory_order_relaxed);
+    const bool pair = p.d == 128 && variant == 2;
+    return (pair ? ra::launch_attn_pair(a, st) : ra::launch_attn_tc(a, st)) == cudaSuccess ? RA_OK
+                                                                                         : RA_ERR_CUDA;
 }
 
 ra_status forward_impl(const Problem &p, const void *q, const void *k, const void *v, void *out,
@@ -282,6 +286,13 @@ ra_status ra_forward_rank_major(const void *q, const void *k, const void *v, voi
 }
 
 unsigned long long ra_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int ra_set_kernel_variant(int variant)
+{
+    if (variant < 0 || variant > 2)
+        return -1;
+    return g_kernel_variant.exchange(variant);
+}
 
 void ra_set_wait_timeout_ns(unsigned long long timeout_ns)
 {

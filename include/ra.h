@@ -218,6 +218,19 @@ ra_status ra_check(ra_stream_t stream);
 const char *ra_status_string(int status);
 
 /*
+ * ra_set_kernel_variant - choose the bf16 tensor-core kernel for the calls
+ * that follow (process-wide): 0 = automatic (the library's default choice),
+ * 1 = one CTA per SM computing two 128-row query tiles, 2 = clusters of two
+ * CTAs sharing each MMA (tcgen05 cta_group::2; head dimension 128 only, other
+ * d use variant 1).  Both compute the same result (same ring order, same
+ * running softmax); they differ in how work maps onto SMs.  Returns the
+ * previous setting, or -1 for an invalid value (nothing changes).
+ * Source: "Ring Attention" page, section "Halka Dikkati Nasil Calisir" (the
+ * per-device blockwise kernel the ring runs).
+ */
+int ra_set_kernel_variant(int variant);
+
+/*
  * ra_set_wait_timeout_ns - bound, in nanoseconds of the GPU's global timer,
  * on every mbarrier wait inside the tensor-core kernel launched after this
  * call (0 restores the default of 4 s).  A wait that runs out records
