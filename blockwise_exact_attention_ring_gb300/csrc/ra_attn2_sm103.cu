@@ -10,12 +10,12 @@
 //   * a cluster of two CTAs runs one work unit (two 128-row query tiles that
 //     share a kv head); CTA r owns query tile r.  One tcgen05.mma with
 //     cta_group::2 computes both tiles at once (M = 256): each CTA holds its
-//     own Q and P in tensor memory (the A operand) and HALF of every K and V
-//     tile in shared memory (the B operand is split along N), so each SM
-//     stages only half the key/value bytes per FLOP;
-//   * with Q in TMEM and one query tile per CTA, tensor memory has room for
-//     two S buffers: S(j + 1) is computed while the softmax of S(j) runs, and
-//     only P(j) -> O += P V waits for the softmax;
+//     own Q tile in shared memory and its P in tensor memory (the A operand)
+//     and HALF of every K and V tile in shared memory (the B operand is split
+//     along N), so each SM stages only half the key/value bytes per FLOP;
+//   * with one query tile per CTA, tensor memory has room for three S
+//     buffers: S(j + 1) and S(j + 2) are computed while the softmax of S(j)
+//     runs, and only P(j) -> O += P V waits for the softmax;
 //   * eight softmax warps per CTA, two per TMEM lane quarter: each thread
 //     owns half a row (64 scores), the two halves exchange their row max
 //     through shared memory each step;
@@ -24,7 +24,13 @@
 //     both CTAs;
 //   * every wait is bounded, as in the single-CTA kernel.
 //
-// TMEM columns per CTA: S0 [0,128), S1 [128,256), O [256,384), Q [384,448).
+// Measured on GB300 this layout is slower than the single-CTA kernel (about
+// 0.6x): each CTA has a single query tile in flight, so its MMA warp waits
+// for every P(j) before it can issue P V(j) and S(j + 3), and the pair MMAs
+// take ~1.7x their isolated issue time in situ.  It is kept as a selectable,
+// parity-tested alternative.
+//
+// TMEM columns per CTA: S/P buffers [0,128), [128,256), [256,384); O [384,512).
 #include <cstdint>
 #include <cstring>
 #include <cuda.h>
@@ -33,7 +39,7 @@
 #include <cudaTypedefs.h>
 
 #include "ra_internal.h"
-#include "ra_ptx.cuh"
+#include "ra_ptx_pair.cuh"
 
 namespace ra {
 
@@ -44,11 +50,14 @@ namespace {
 constexpr int P_THREADS = 384;  // warps: 0 TMA, 1 MMA + TMEM, 2-3 spare, 4-11 softmax
 constexpr int P_D = 128;
 constexpr uint32_t P_TMEM_COLS = 512;
-constexpr uint32_t COL_O = 256, COL_Q = 384;
+constexpr int NSB = 3;              // S / P buffers in TMEM
+constexpr uint32_t COL_O = 384;
 constexpr int KST = 4, VST = 4;
 constexpr int K_HALF = 64 * 128 * 2;   // 64 keys x 128 d: two 8 KB swizzled slabs
 constexpr int V_HALF = 128 * 64 * 2;   // 128 keys x 64 d: one 16 KB swizzled slab
-constexpr int OFF_K = 0;
+constexpr int Q_TILE = 128 * 128 * 2;  // this CTA's query tile: two 16 KB swizzled slabs
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + Q_TILE;
 constexpr int OFF_V = OFF_K + KST * K_HALF;
 constexpr int OFF_X = OFF_V + VST * V_HALF;  // half-row exchange: 3 buffers x 2 halves x 128 floats
 constexpr int OFF_CTRL = OFF_X + 3 * 2 * 128 * 4;
@@ -57,22 +66,22 @@ constexpr float P_LAZY_LOG2 = 8.0f;
 constexpr float P_LN2 = 0.693147180559945309f;
 
 enum : unsigned int {
-    PS_K_EMPTY = 21, PS_V_EMPTY, PS_K_FULL, PS_V_FULL, PS_P_FULL, PS_Q_READY, PS_S_FULL,
+    PS_K_EMPTY = 21, PS_V_EMPTY, PS_K_FULL, PS_V_FULL, PS_P_FULL, PS_O_FREE, PS_S_FULL,
+    PS_Q_EMPTY, PS_Q_FULL,
     PS_O_DONE, PS_XCH, PS_DRAIN
 };
 
 struct PairCtrl {
     uint64_t k_full[KST], k_empty[KST], v_full[VST], v_empty[VST];
-    uint64_t s_full[2], p_full[2], o_done[2], q_ready, xch[3], final_bar;
+    uint64_t s_full[NSB], p_full[NSB], o_done[NSB], o_free, q_full, q_empty, xch[3], final_bar;
     uint32_t tmem_base;
     int abort;
 };
 static_assert(sizeof(PairCtrl) <= 512, "control block");
 
 struct PairParams {
-    CUtensorMap tm_k, tm_v;
+    CUtensorMap tm_q, tm_k, tm_v;
     RaUnitSpace sp;
-    const __nv_bfloat16 *q;
     void *out;
     float *lse;
     long long q_rows;  // B * H * S
@@ -132,27 +141,6 @@ __device__ __forceinline__ void pdrain(uint32_t bar, uint32_t parity, uint64_t t
     mbar_wait_cluster(bar, parity, &never, tmo, &g_ra_status, PS_DRAIN);
 }
 
-// Store this thread's half row of Q (64 bf16 = 32 TMEM columns) into the Q
-// region; rows past the tensor read as zero.
-__device__ __forceinline__ void store_q_half(const PairParams &p, uint32_t tq, long long qrow, int h)
-{
-    uint32_t w[32];
-    if (qrow < p.q_rows) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.q + qrow * P_D + h * 64);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const uint4 v = src[c];
-            w[4 * c] = v.x, w[4 * c + 1] = v.y, w[4 * c + 2] = v.z, w[4 * c + 3] = v.w;
-        }
-    } else {
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-            w[c] = 0u;
-    }
-    __syncwarp();  // reconverge before the warp-collective store
-    tmem_st32(tq + h * 32, w);
-}
-
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
 ra_attn_pair_kernel(const __grid_constant__ PairParams p)
 {
@@ -178,20 +166,23 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
             mbar_init(bar(ctrl->v_full[s]), 1);
             mbar_init(bar(ctrl->v_empty[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NSB; ++b) {
             mbar_init(bar(ctrl->s_full[b]), 1);
             mbar_init(bar(ctrl->p_full[b]), 16);  // 8 softmax warps x 2 CTAs
-            mbar_init(bar(ctrl->o_done[b]), 1);   // P V of even / odd key tiles
+            mbar_init(bar(ctrl->o_done[b]), 1);   // P V of key tiles j with j % NSB == b
         }
         for (int b = 0; b < 3; ++b)
             mbar_init(bar(ctrl->xch[b]), 8);      // this CTA's softmax warps
-        mbar_init(bar(ctrl->q_ready), 16);
+        mbar_init(bar(ctrl->o_free), 16);  // epilogues of both CTAs read O
+        mbar_init(bar(ctrl->q_full), 1);
+        mbar_init(bar(ctrl->q_empty), 1);
         mbar_init(bar(ctrl->final_bar), 1);
         ctrl->abort = 0;
         fence_mbar_init();
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&p.tm_q);
         tma_prefetch_desc(&p.tm_k);
         tma_prefetch_desc(&p.tm_v);
     }
@@ -212,13 +203,26 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
         // ------------------------------------------------------------ producer (both CTAs)
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_last();
-            uint32_t kcnt = 0, vcnt = 0;
+            const uint64_t pol_q = l2_policy_evict_first();
+            uint32_t kcnt = 0, vcnt = 0, qcnt = 0;
             bool ok = true;
             for (int r = 0; ok; ++r) {
                 const int u = pair_unit_index(r, cluster, G);
                 if (u >= p.n_units)
                     break;
                 const RaUnit U = ra_unit_decode(p.sp, u);
+                // this CTA's query tile, once the previous unit's S MMAs are done
+                if (qcnt > 0 && !(ok = pwait(bar(ctrl->q_empty), (qcnt - 1) & 1, abort, tmo, PS_Q_EMPTY)))
+                    break;
+                if (leader)
+                    mbar_arrive_expect_tx(bar(ctrl->q_full), 2 * Q_TILE);
+                {
+                    const int qbh = crank ? U.bh1 : U.bh0, qta = crank ? U.ta1 : U.ta0;
+                    const int qrow = qbh * p.S + U.rank * p.L + qta * RA_TILE;
+                    tma_load_2d_pair(sb + OFF_Q, &p.tm_q, 0, qrow, lbar(ctrl->q_full), pol_q);
+                    tma_load_2d_pair(sb + OFF_Q + Q_TILE / 2, &p.tm_q, 64, qrow, lbar(ctrl->q_full), pol_q);
+                }
+                ++qcnt;
                 const int b = U.bh0 / p.H;
                 const int kvbh = b * p.Hkv + (U.bh0 - b * p.H) / group;
                 Walk w;
@@ -268,9 +272,11 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
             constexpr uint32_t IDESC_PV = idesc_bf16_f32(256, P_D, 1);
             auto issue_s = [&](int buf, int ks) {
                 const uint32_t kb = sb + OFF_K + ks * K_HALF;
+                const uint32_t qb = sb + OFF_Q;
 #pragma unroll
                 for (int kk = 0; kk < P_D / 16; ++kk)
-                    mma_ts_pair(tmem + buf * 128, tmem + COL_Q + kk * 8,
+                    mma_ss_pair(tmem + buf * 128,
+                                smem_desc_sw128(qb + (kk >> 2) * (Q_TILE / 2) + (kk & 3) * 32, 16, 1024),
                                 smem_desc_sw128(kb + (kk >> 2) * (K_HALF / 2) + (kk & 3) * 32, 16, 1024),
                                 IDESC_S, kk > 0);
             };
@@ -282,19 +288,18 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
                                 smem_desc_sw128(vb + kk * 2048, V_HALF, 1024), IDESC_PV,
                                 (acc || kk > 0) ? 1u : 0u);
             };
-            uint32_t kcnt = 0, vcnt = 0, qcnt = 0, pcnt[2] = {0, 0};
+            uint32_t kcnt = 0, vcnt = 0, qcnt = 0, pcnt[NSB] = {0, 0, 0};
             bool ok = true;
             for (int r = 0; ok; ++r) {
                 const int u = pair_unit_index(r, cluster, G);
                 if (u >= p.n_units)
                     break;
                 const int n = ra_unit_decode(p.sp, u).cost;
-                // both CTAs stored this unit's Q (and read out the previous O)
-                if (!(ok = pwait(bar(ctrl->q_ready), qcnt & 1, abort, tmo, PS_Q_READY)))
+                // both CTAs' query tiles are in shared memory
+                if (!(ok = pwait(bar(ctrl->q_full), qcnt & 1, abort, tmo, PS_Q_FULL)))
                     break;
-                ++qcnt;
                 tc_fence_after();
-                const int pre = n < 2 ? n : 2;
+                const int pre = n < NSB ? n : NSB;
                 for (int jj = 0; jj < pre && ok; ++jj) {
                     const int ks = kcnt % KST;
                     if (!(ok = pwait(bar(ctrl->k_full[ks]), (kcnt / KST) & 1, abort, tmo, PS_K_FULL)))
@@ -305,8 +310,14 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
                     mma_commit_pair(bar(ctrl->k_empty[ks]));
                     ++kcnt;
                 }
+                if (n <= NSB)
+                    mma_commit_pair(bar(ctrl->q_empty));  // last S of the unit issued
+                // the previous unit's O has been read by both epilogues
+                if (ok && qcnt > 0 && !(ok = pwait(bar(ctrl->o_free), (qcnt - 1) & 1, abort, tmo, PS_O_FREE)))
+                    break;
+                ++qcnt;
                 for (int j = 0; j < n && ok; ++j) {
-                    const int buf = j & 1;
+                    const int buf = j % NSB;
                     const int vs = vcnt % VST;
                     if (!(ok = pwait(bar(ctrl->v_full[vs]), (vcnt / VST) & 1, abort, tmo, PS_V_FULL)))
                         break;
@@ -318,8 +329,8 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
                     mma_commit_pair(bar(ctrl->o_done[buf]));
                     mma_commit_pair(bar(ctrl->v_empty[vs]));
                     ++vcnt;
-                    if (j + 2 < n) {
-                        // S(j + 2) reuses this buffer; the tensor pipe runs in
+                    if (j + NSB < n) {
+                        // S(j + NSB) reuses this buffer; the tensor pipe runs in
                         // issue order, so P(j) is read before it is overwritten
                         const int ks = kcnt % KST;
                         if (!(ok = pwait(bar(ctrl->k_full[ks]), (kcnt / KST) & 1, abort, tmo, PS_K_FULL)))
@@ -329,6 +340,8 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
                         mma_commit_pair(bar(ctrl->s_full[buf]));
                         mma_commit_pair(bar(ctrl->k_empty[ks]));
                         ++kcnt;
+                        if (j + NSB + 1 == n)
+                            mma_commit_pair(bar(ctrl->q_empty));  // last S of the unit issued
                     }
                 }
             }
@@ -343,9 +356,9 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
         const uint32_t tbase = tmem + ((uint32_t)(qw * 32) << 16);
         const float sl2 = p.scale_log2;
         // s_full[b] completes once per S into buffer b; o_done[b] once per P V
-        // of a key tile with index parity b; xch[0..1] alternate over all
+        // of a key tile j with j % NSB == b; xch[0..1] alternate over all
         // steps, xch[2] serves the epilogue
-        uint32_t scnt[2] = {0, 0}, pvdone[2] = {0, 0}, gstep = 0, ecnt = 0;
+        uint32_t scnt[NSB] = {0, 0, 0}, pvdone[NSB] = {0, 0, 0}, gstep = 0, ecnt = 0;
         bool ok = true;
         // Exchange one float per half row with the partner thread (the other
         // column half of the same row, in warp w +- 4); returns the partner's.
@@ -361,17 +374,6 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
             return true;
         };
         int u = pair_unit_index(0, cluster, G);
-        if (u < p.n_units) {
-            // the first unit's Q; later ones are stored after each epilogue
-            const RaUnit U = ra_unit_decode(p.sp, u);
-            const int bh = crank ? U.bh1 : U.bh0, ta = crank ? U.ta1 : U.ta0;
-            store_q_half(p, tbase + COL_Q, (long long)bh * p.S + (long long)U.rank * p.L + ta * RA_TILE + row, h);
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive_cluster(lbar(ctrl->q_ready));
-        }
         for (int rr = 0; ok && u < p.n_units; ++rr, u = pair_unit_index(rr, cluster, G)) {
             const RaUnit U = ra_unit_decode(p.sp, u);
             const int bh = crank ? U.bh1 : U.bh0;
@@ -383,7 +385,7 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
             w.start(U.rank, max(U.ta0, U.ta1), p);
             int jj = 0;
             for (; w.valid(); w.advance(), ++jj, ++gstep) {
-                const int buf = jj & 1;
+                const int buf = jj % NSB;
                 if (!(ok = pwait_warp(bar(ctrl->s_full[buf]), scnt[buf] & 1, abort, tmo, PS_S_FULL)))
                     break;
                 ++scnt[buf];
@@ -420,11 +422,11 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
                 __syncwarp();
                 if (jj > 0 && __any_sync(0xffffffffu, resc)) {
                     // O must hold P V of the previous key tile before it is
-                    // rescaled.  S(jj) completing implies P V(jj - 2) did, so
-                    // o_done[(jj - 1) & 1] is either one completion short or
+                    // rescaled.  S(jj) completing implies P V(jj - NSB) did, so
+                    // o_done[(jj - 1) % NSB] is either one completion short or
                     // done: a parity wait is unambiguous.
-                    const int pb = (jj - 1) & 1;
-                    const uint32_t idx = pvdone[pb] + (uint32_t)((jj - 1) >> 1);
+                    const int pb = (jj - 1) % NSB;
+                    const uint32_t idx = pvdone[pb] + (uint32_t)((jj - 1) / NSB);
                     if (!(ok = pwait_warp(bar(ctrl->o_done[pb]), idx & 1, abort, tmo, PS_O_DONE)))
                         break;
                     tc_fence_after();
@@ -470,13 +472,13 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
             // ------------------------------------------------ epilogue
             const int n = jj;
             {
-                const int pb = (n - 1) & 1;
-                const uint32_t idx = pvdone[pb] + (uint32_t)((n - 1) >> 1);
+                const int pb = (n - 1) % NSB;
+                const uint32_t idx = pvdone[pb] + (uint32_t)((n - 1) / NSB);
                 if (!(ok = pwait_warp(bar(ctrl->o_done[pb]), idx & 1, abort, tmo, PS_O_DONE)))
                     break;
             }
-            pvdone[0] += (uint32_t)((n + 1) >> 1);
-            pvdone[1] += (uint32_t)(n >> 1);
+            for (int b2 = 0; b2 < NSB; ++b2)
+                pvdone[b2] += (uint32_t)((n - b2 + NSB - 1) / NSB);  // j < n with j % NSB == b2
             tc_fence_after();
             float l_other;
             if (!(ok = exchange(2, ecnt & 1, l_run, l_other)))
@@ -516,20 +518,11 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
             }
             if (valid && h == 0)
                 p.lse[orow] = l_row > 0.f ? (m_run + log2f(l_row)) * P_LN2 : -INFINITY;
-            __syncwarp();
-            // next unit's Q (all MMAs of this unit are done: its last P V was)
-            const int un = pair_unit_index(rr + 1, cluster, G);
-            if (un < p.n_units) {
-                const RaUnit N2 = ra_unit_decode(p.sp, un);
-                const int bh2 = crank ? N2.bh1 : N2.bh0, ta2 = crank ? N2.ta1 : N2.ta0;
-                store_q_half(p, tbase + COL_Q,
-                             (long long)bh2 * p.S + (long long)N2.rank * p.L + ta2 * RA_TILE + row, h);
-                tmem_wait_st();
-            }
+            // O has been read: the next unit's first P V may overwrite it
             tc_fence_before();
             __syncwarp();
-            if (lane == 0 && un < p.n_units)
-                mbar_arrive_cluster(lbar(ctrl->q_ready));
+            if (lane == 0)
+                mbar_arrive_cluster(lbar(ctrl->o_free));
         }
     }
     // ---------------------------------------------------------------- teardown
@@ -594,13 +587,13 @@ cudaError_t launch_attn_pair(const TcLaunch &a, cudaStream_t st)
     PairParams p;
     memset(&p, 0, sizeof(p));
     const long long kv_rows = (long long)a.B * a.Hkv * a.S;
-    if (!encode_box(&p.tm_k, a.k, kv_rows, 64) || !encode_box(&p.tm_v, a.v, kv_rows, RA_TILE))
+    if (!encode_box(&p.tm_q, a.q, (long long)a.B * a.H * a.S, RA_TILE) ||
+        !encode_box(&p.tm_k, a.k, kv_rows, 64) || !encode_box(&p.tm_v, a.v, kv_rows, RA_TILE))
         return cudaErrorInvalidValue;
     p.sp = ra_unit_space(a.B, a.H, a.Hkv, a.S, a.N, a.layout, a.causal, a.s_begin, a.s_end);
     const long long n_units = ra_unit_count(p.sp);
     if (n_units > 0x7fffffffll)
         return cudaErrorInvalidValue;
-    p.q = static_cast<const __nv_bfloat16 *>(a.q);
     p.out = a.out;
     p.lse = a.lse;
     p.q_rows = (long long)a.B * a.H * a.S;
