@@ -5,11 +5,11 @@ The compute path is the C-ABI library ``libra.so`` built from ``csrc/`` (see
 package does not load the library; the first compute call does, and raises if
 the library has not been built (``build.build()``).
 """
-from . import inputs  # noqa: F401
-from .binding import (RaError, check, forward, lib, merge, permute,  # noqa: F401
-                      schedule_stats, schedule_units, set_kernel_variant, status_string,
-                      version, workspace_bytes)
+from . import balance, inputs  # noqa: F401
+from .binding import (RaError, all_to_all, block_units, check, forward, forward_block,  # noqa: F401
+                      forward_ulysses, lib, merge, permute, schedule_stats, schedule_units,
+                      set_kernel_variant, status_string, version, workspace_bytes)
 
-__all__ = ["inputs", "RaError", "check", "forward", "lib", "merge", "permute",
-           "schedule_stats", "schedule_units", "set_kernel_variant", "status_string", "version",
-           "workspace_bytes"]
+__all__ = ["balance", "inputs", "RaError", "all_to_all", "block_units", "check", "forward",
+           "forward_block", "forward_ulysses", "lib", "merge", "permute", "schedule_stats",
+           "schedule_units", "set_kernel_variant", "status_string", "version", "workspace_bytes"]

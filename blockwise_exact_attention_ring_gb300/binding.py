@@ -22,7 +22,7 @@ HEADER = os.path.join(HERE, "..", "include", "ra.h")
 RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA = 0, 1, 2, 3
 RA_ERR_NO_MEMORY, RA_ERR_TIMEOUT, RA_ERR_WORKSPACE, RA_ERR_SCRATCH_LIMIT = 4, 5, 6, 7
 LAYOUTS = {"contiguous": 0, "striped": 1}
-MODES = {"fused": 0, "per_step": 1}
+MODES = {"fused": 0, "per_step": 1, "ring": 2}
 DTYPES = {torch.bfloat16: 0, torch.float32: 1}
 
 _lib = None
@@ -55,6 +55,11 @@ def lib():
     L.ra_workspace_bytes.restype = sz
     L.ra_forward_ws.argtypes = [vp] * 5 + [i] * 10 + [vp, sz, vp]
     L.ra_forward_rank_major.argtypes = [vp] * 5 + [i] * 10 + [vp, sz, vp]
+    L.ra_forward_block.argtypes = [vp] * 5 + [i] * 11 + [vp]
+    L.ra_all_to_all.argtypes = [vp, vp] + [i] * 7 + [vp]
+    L.ra_ulysses_workspace_bytes.argtypes = [i] * 8
+    L.ra_ulysses_workspace_bytes.restype = sz
+    L.ra_forward_ulysses.argtypes = [vp] * 5 + [i] * 8 + [vp, sz, vp]
     L.ra_permute.argtypes = [vp, vp] + [i] * 7 + [vp]
     L.ra_merge.argtypes = [vp] * 4 + [ll, i, vp]
     L.ra_check.argtypes = [vp]
@@ -70,10 +75,13 @@ def lib():
     L.ra_launch_count.restype = ctypes.c_ulonglong
     L.ra_schedule_units.argtypes = [i] * 9 + [vp, ll]
     L.ra_schedule_units.restype = ll
+    L.ra_schedule_block_units.argtypes = [i] * 9 + [vp, ll]
+    L.ra_schedule_block_units.restype = ll
     L.ra_schedule_stats.argtypes = [i, i, i, i, vp, vp]
     L.ra_schedule_stats.restype = ll
     for fn in ("ra_forward", "ra_forward_f32", "ra_forward_noalloc", "ra_forward_ws",
-               "ra_forward_rank_major", "ra_permute", "ra_merge", "ra_check"):
+               "ra_forward_rank_major", "ra_forward_block", "ra_all_to_all", "ra_forward_ulysses",
+               "ra_permute", "ra_merge", "ra_check"):
         getattr(L, fn).restype = i
     _lib = L
     return L
@@ -220,6 +228,90 @@ def schedule_units(B, H, Hkv, S, n_blocks, layout="contiguous", causal=False, st
     L.ra_schedule_units(B, H, Hkv, S, n_blocks, LAYOUTS[layout], int(bool(causal)), s0, s1,
                         out.ctypes.data, n)
     return out
+
+
+def block_units(B, H, Hkv, S, n_blocks, layout, causal, rank, step):
+    """Work units ra_forward_block launches for (rank, step), same format as
+    schedule_units."""
+    L = lib()
+    args = (B, H, Hkv, S, n_blocks, LAYOUTS[layout], int(bool(causal)), rank, step)
+    n = L.ra_schedule_block_units(*args, None, 0)
+    if n < 0:
+        raise ValueError("invalid schedule request")
+    out = np.zeros((n, 8), dtype=np.int32)
+    L.ra_schedule_block_units(*args, out.ctypes.data, n)
+    return out
+
+
+def forward_block(q, k, v, out_s, lse_s, n_blocks, rank, step, layout="contiguous", causal=False,
+                  stream=None):
+    """One device's ring step (ra_forward_block): writes the fp32 partial of
+    query block `rank` against key/value block (rank - step) mod n_blocks into
+    the rows of that block in out_s [B,H,S,d] and lse_s [B,H,S].  q, k, v are
+    in the layout's rank-major order."""
+    B, H, Hkv, S, d = _dims(q, k, v)
+    if out_s.dtype != torch.float32 or lse_s.dtype != torch.float32:
+        raise ValueError("out_s and lse_s must be float32")
+    if tuple(out_s.shape) != (B, H, S, d) or tuple(lse_s.shape) != (B, H, S):
+        raise ValueError("out_s must be [B,H,S,d] and lse_s [B,H,S]")
+    if not (out_s.is_contiguous() and lse_s.is_contiguous()):
+        raise ValueError("out_s and lse_s must be contiguous")
+    st = lib().ra_forward_block(_p(q), _p(k), _p(v), _p(out_s), _p(lse_s), B, H, Hkv, S, d, n_blocks,
+                                LAYOUTS[layout], int(bool(causal)), DTYPES[q.dtype], int(rank),
+                                int(step), _stream(stream))
+    _check(st, "ra_forward_block")
+
+
+def all_to_all(x: torch.Tensor, n_dev: int, inverse: bool = False,
+               out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Ulysses all-to-all (ra_all_to_all): sequence-sharded [n_dev, B, Hn, L, d]
+    -> head-sharded [n_dev, B, Hn/n_dev, S, d], or back with inverse=True.
+    Per-row values (lse) drop the trailing d axis."""
+    if not x.is_cuda or not x.is_contiguous() or x.dim() not in (4, 5):
+        raise ValueError("x must be a contiguous CUDA tensor of 5 (or 4, for per-row values) dims")
+    per_row = x.dim() == 4
+    n, B = x.shape[0], x.shape[1]
+    d = 1 if per_row else x.shape[4]
+    if n != n_dev:
+        raise ValueError("dim 0 must be n_dev")
+    if not inverse:
+        Hn, S = x.shape[2], x.shape[3] * n_dev
+        shape = (n_dev, B, Hn // n_dev, S) + (() if per_row else (d,))
+    else:
+        Hn, S = x.shape[2] * n_dev, x.shape[3]
+        shape = (n_dev, B, Hn, S // n_dev) + (() if per_row else (d,))
+    if out is None:
+        out = torch.empty(shape, dtype=x.dtype, device=x.device)
+    _check(lib().ra_all_to_all(_p(x), _p(out), B, Hn, S, d, x.element_size(), n_dev, int(bool(inverse)),
+                               _stream(stream)), "ra_all_to_all")
+    return out
+
+
+def forward_ulysses(q, k, v, n_dev: int, causal: bool = False, workspace=None, stream=None):
+    """Ulysses attention over n_dev emulated devices (ra_forward_ulysses).
+    q [n_dev, B, H, L, d], k/v [n_dev, B, Hkv, L, d] sequence shards; returns
+    (out [n_dev, B, H, L, d], lse fp32 [n_dev, B, H, L])."""
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous() or t.dim() != 5:
+            raise ValueError("q, k, v must be contiguous CUDA tensors [n_dev, B, heads, L, d]")
+    n, B, H, Ls, d = q.shape
+    Hkv = k.shape[2]
+    if n != n_dev or v.shape != k.shape or k.shape[0] != n or k.shape[1] != B or k.shape[3:] != q.shape[3:]:
+        raise ValueError("shard shapes do not match")
+    if q.dtype not in DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share a supported dtype")
+    S = Ls * n_dev
+    L = lib()
+    nbytes = int(L.ra_ulysses_workspace_bytes(B, H, Hkv, S, d, n_dev, int(bool(causal)), DTYPES[q.dtype]))
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    out = torch.empty_like(q)
+    lse = torch.empty(n_dev, B, H, Ls, device=q.device, dtype=torch.float32)
+    _check(L.ra_forward_ulysses(_p(q), _p(k), _p(v), _p(out), _p(lse), B, H, Hkv, S, d, n_dev,
+                                int(bool(causal)), DTYPES[q.dtype], _p(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream)),
+           "ra_forward_ulysses")
+    return out, lse
 
 
 def set_kernel_variant(variant: int) -> int:

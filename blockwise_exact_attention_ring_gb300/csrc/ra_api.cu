@@ -70,7 +70,7 @@ ra_status check_problem(const Problem &p)
         return RA_ERR_INVALID_ARG;
     if (p.dtype != RA_DTYPE_BF16 && p.dtype != RA_DTYPE_F32)
         return RA_ERR_INVALID_ARG;
-    if (p.mode != RA_MODE_FUSED && p.mode != RA_MODE_PER_STEP)
+    if (p.mode != RA_MODE_FUSED && p.mode != RA_MODE_PER_STEP && p.mode != RA_MODE_RING)
         return RA_ERR_INVALID_ARG;
     // 32-bit TMA row coordinates and grid limits
     if ((long long)p.B * p.H * p.S >= (1ll << 31) || (long long)p.B * p.H > 65535)
@@ -79,7 +79,7 @@ ra_status check_problem(const Problem &p)
         return RA_ERR_UNSUPPORTED;
     if (p.dtype == RA_DTYPE_F32 && p.d > 256)
         return RA_ERR_UNSUPPORTED;
-    if (p.mode == RA_MODE_PER_STEP && p.d % 4 != 0)
+    if (p.mode != RA_MODE_FUSED && p.d % 4 != 0)
         return RA_ERR_UNSUPPORTED;
     return RA_OK;
 }
@@ -87,9 +87,11 @@ ra_status check_problem(const Problem &p)
 // Workspace layout (each region 256-byte aligned):
 //   striped:            q', k', v' in striped order
 //   striped and fused:  out', lse' in striped order
-//   per-step:           running out/lse (fp32) and step partial out/lse (fp32)
+//   per-step and ring:  running out/lse (fp32) and step partial out/lse (fp32)
+//   ring:               two rotating copies of k and v (rank-major order)
 struct WsLayout {
     size_t q = 0, k = 0, v = 0, out = 0, lse = 0, run = 0, run_lse = 0, part = 0, part_lse = 0;
+    size_t ring_k[2] = {0, 0}, ring_v[2] = {0, 0};
     size_t total = 0;
 };
 
@@ -111,11 +113,17 @@ WsLayout ws_layout(const Problem &p)
             w.lse = take(p.rows() * 4);
         }
     }
-    if (p.mode == RA_MODE_PER_STEP) {
+    if (p.mode != RA_MODE_FUSED) {
         w.run = take(p.q_elems() * 4);
         w.run_lse = take(p.rows() * 4);
         w.part = take(p.q_elems() * 4);
         w.part_lse = take(p.rows() * 4);
+    }
+    if (p.mode == RA_MODE_RING && p.N > 1) {
+        for (int b = 0; b < 2; ++b) {
+            w.ring_k[b] = take(p.kv_elems() * p.esz());
+            w.ring_v[b] = take(p.kv_elems() * p.esz());
+        }
     }
     w.total = off;
     return w;
@@ -123,11 +131,15 @@ WsLayout ws_layout(const Problem &p)
 
 // ------------------------------------------------------------------ forward
 ra_status attention_pass(const Problem &p, const void *q, const void *k, const void *v, void *out,
-                         float *lse, int s_begin, int s_end, bool out_f32, int sm, cudaStream_t st)
+                         float *lse, int s_begin, int s_end, bool out_f32, int sm, cudaStream_t st,
+                         int rank_lo = 0, int rank_hi = -1)
 {
+    if (rank_hi < 0)
+        rank_hi = p.N;
     if (p.dtype == RA_DTYPE_F32) {
         ra::launch_attn_f32((const float *)q, (const float *)k, (const float *)v, (float *)out, lse,
-                            p.B, p.H, p.Hkv, p.S, p.d, p.N, p.layout, p.causal, s_begin, s_end, st);
+                            p.B, p.H, p.Hkv, p.S, p.d, p.N, p.layout, p.causal, s_begin, s_end, rank_lo,
+                            rank_hi, st);
         count_launch();
         return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
     }
@@ -135,16 +147,150 @@ ra_status attention_pass(const Problem &p, const void *q, const void *k, const v
     a.q = q, a.k = k, a.v = v, a.out = out, a.lse = lse;
     a.B = p.B, a.H = p.H, a.Hkv = p.Hkv, a.S = p.S, a.d = p.d, a.N = p.N;
     a.layout = p.layout, a.causal = p.causal, a.s_begin = s_begin, a.s_end = s_end;
+    a.rank_lo = rank_lo, a.rank_hi = rank_hi;
     a.out_f32 = out_f32 ? 1 : 0;
     a.timeout_ns = g_timeout_ns;
     a.sm_count = sm;
-    if (ra_unit_count(ra_unit_space(p.B, p.H, p.Hkv, p.S, p.N, p.layout, p.causal, s_begin, s_end)) > 0)
+    if (ra_unit_count(ra_unit_space_ranks(ra_unit_space(p.B, p.H, p.Hkv, p.S, p.N, p.layout, p.causal,
+                                                        s_begin, s_end),
+                                          rank_lo, rank_hi)) > 0)
         count_launch();
     const int variant = g_kernel_variant.load(std::memory_order_relaxed);
     const bool pair = p.d == 128 && variant == 2;
     return (pair ? ra::launch_attn_pair(a, st) : ra::launch_attn_tc(a, st)) == cudaSuccess ? RA_OK
                                                                                          : RA_ERR_CUDA;
 }
+
+// ------------------------------------------------------------------ ring copies
+// The copy stream of each device: created once, non-blocking, lives as long
+// as the process.
+cudaStream_t copy_stream()
+{
+    static std::mutex mu;
+    static std::vector<cudaStream_t> streams;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if ((int)streams.size() <= dev)
+        streams.resize(dev + 1, nullptr);
+    if (!streams[dev] && cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess) {
+        cudaGetLastError();
+        streams[dev] = nullptr;
+    }
+    return streams[dev];
+}
+
+// Key/value rotation of RA_MODE_RING.  Buffers R[0], R[1] hold the blocks in
+// natural block positions: at step t >= 1 every rank i reads block
+// j = (i - t) mod N, which the copy for step t moved there from the buffer of
+// step t - 1 (where rank i - 1 held it).  Step 0 reads the inputs.  Copy t
+// writes R[(t - 1) % 2], last read by step t - 2, so it waits for that step;
+// it runs on the copy stream while step t - 1 computes.
+struct RingCopies {
+    const Problem *p = nullptr;
+    cudaStream_t cs = nullptr;
+    const char *k0 = nullptr, *v0 = nullptr;
+    char *rk[2] = {nullptr, nullptr}, *rv[2] = {nullptr, nullptr};
+    std::vector<cudaEvent_t> copied, computed;
+    cudaEvent_t fork = nullptr, join = nullptr;
+
+    ~RingCopies()
+    {
+        for (cudaEvent_t e : copied)
+            if (e)
+                cudaEventDestroy(e);
+        for (cudaEvent_t e : computed)
+            if (e)
+                cudaEventDestroy(e);
+        if (fork)
+            cudaEventDestroy(fork);
+        if (join)
+            cudaEventDestroy(join);
+    }
+
+    bool make(cudaEvent_t &e) { return cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess; }
+
+    // copy t: every rank's block for step t into R[(t - 1) % 2]
+    bool copy(int t)
+    {
+        const Problem &P = *p;
+        const size_t row = (size_t)P.d * P.esz(), blk = (size_t)P.L() * row, pitch = (size_t)P.S * row;
+        const size_t rows = (size_t)P.B * P.Hkv;
+        const char *sk = t == 1 ? k0 : rk[t % 2], *sv = t == 1 ? v0 : rv[t % 2];
+        char *dk = rk[(t - 1) % 2], *dv = rv[(t - 1) % 2];
+        if (t >= 3 && cudaStreamWaitEvent(cs, computed[t - 2], 0) != cudaSuccess)
+            return false;
+        for (int i = 0; i < P.N; ++i) {
+            const size_t off = (size_t)ra_ring_block(i, t, P.N) * blk;  // block rank i receives
+            if (cudaMemcpy2DAsync(dk + off, pitch, sk + off, pitch, blk, rows, cudaMemcpyDeviceToDevice, cs) !=
+                    cudaSuccess ||
+                cudaMemcpy2DAsync(dv + off, pitch, sv + off, pitch, blk, rows, cudaMemcpyDeviceToDevice, cs) !=
+                    cudaSuccess)
+                return false;
+        }
+        return cudaEventRecord(copied[t], cs) == cudaSuccess;
+    }
+
+    ra_status begin(const Problem &P, const void *k, const void *v, char *base, const WsLayout &w,
+                    cudaStream_t st)
+    {
+        p = &P;
+        k0 = static_cast<const char *>(k), v0 = static_cast<const char *>(v);
+        if (P.N == 1)
+            return RA_OK;
+        for (int b = 0; b < 2; ++b)
+            rk[b] = base + w.ring_k[b], rv[b] = base + w.ring_v[b];
+        cs = copy_stream();
+        if (!cs)
+            return RA_ERR_CUDA;
+        copied.assign(P.N, nullptr), computed.assign(P.N, nullptr);
+        for (int s = 0; s < P.N; ++s)
+            if (!make(copied[s]) || !make(computed[s]))
+                return RA_ERR_CUDA;
+        if (!make(fork) || !make(join))
+            return RA_ERR_CUDA;
+        // the copy stream starts after everything already on st (the inputs)
+        if (cudaEventRecord(fork, st) != cudaSuccess || cudaStreamWaitEvent(cs, fork, 0) != cudaSuccess)
+            return RA_ERR_CUDA;
+        return copy(1) ? RA_OK : RA_ERR_CUDA;
+    }
+
+    // K and V that step s reads; waits on st for their copy
+    ra_status before_step(int s, const void **k, const void **v, cudaStream_t st)
+    {
+        if (s == 0 || p->N == 1) {
+            *k = k0, *v = v0;
+            return RA_OK;
+        }
+        if (cudaStreamWaitEvent(st, copied[s], 0) != cudaSuccess)
+            return RA_ERR_CUDA;
+        *k = rk[(s - 1) % 2], *v = rv[(s - 1) % 2];
+        return RA_OK;
+    }
+
+    // after step s's launches: record it, start the copy for step s + 2
+    ra_status after_step(int s, cudaStream_t st)
+    {
+        if (p->N == 1)
+            return RA_OK;
+        if (cudaEventRecord(computed[s], st) != cudaSuccess)
+            return RA_ERR_CUDA;
+        if (s + 2 < p->N && !copy(s + 2))
+            return RA_ERR_CUDA;
+        return RA_OK;
+    }
+
+    // st waits for the copy stream (no copy outlives the call's stream order)
+    ra_status end(cudaStream_t st)
+    {
+        if (p->N == 1)
+            return RA_OK;
+        if (cudaEventRecord(join, cs) != cudaSuccess || cudaStreamWaitEvent(st, join, 0) != cudaSuccess)
+            return RA_ERR_CUDA;
+        return RA_OK;
+    }
+};
 
 ra_status forward_impl(const Problem &p, const void *q, const void *k, const void *v, void *out,
                        float *lse, void *ws, size_t ws_bytes, cudaStream_t st)
@@ -197,25 +343,37 @@ ra_status forward_impl(const Problem &p, const void *q, const void *k, const voi
         return RA_OK;
     }
 
-    // per-step: step 0 initialises the running state, later steps are merged
+    // per-step and ring: step 0 initialises the running state, later steps
+    // are merged
     float *run = (float *)(base + w.run), *run_lse = (float *)(base + w.run_lse);
     float *part = (float *)(base + w.part), *part_lse = (float *)(base + w.part_lse);
-    rs = attention_pass(p, qk, kk, vk, run, run_lse, 0, 1, true, sm, st);
-    if (rs != RA_OK)
-        return rs;
     const long long L = p.L();
-    for (int s = 1; s < p.N; ++s) {
-        rs = attention_pass(p, qk, kk, vk, part, part_lse, s, s + 1, true, sm, st);
+    const bool ring = p.mode == RA_MODE_RING;
+    RingCopies rc;
+    if (ring && (rs = rc.begin(p, kk, vk, base, w, st)) != RA_OK)
+        return rs;
+    for (int s = 0; s < p.N; ++s) {
+        const void *ks = kk, *vs = vk;
+        if (ring && (rs = rc.before_step(s, &ks, &vs, st)) != RA_OK)
+            return rs;
+        rs = attention_pass(p, qk, ks, vs, s == 0 ? run : part, s == 0 ? run_lse : part_lse, s, s + 1, true,
+                            sm, st);
         if (rs != RA_OK)
             return rs;
-        // contiguous causal: at step s only ranks i >= s hold a visible block
-        const long long begin = (p.causal && p.layout == RA_LAYOUT_CONTIGUOUS) ? s * L : 0;
-        ra::launch_merge(run, run_lse, part, part_lse, (long long)p.B * p.H, p.S, begin, p.S - begin,
-                         p.d, sm, st);
-        count_launch();
-        if (cudaGetLastError() != cudaSuccess)
-            return RA_ERR_CUDA;
+        if (s > 0) {
+            // contiguous causal: at step s only ranks i >= s hold a visible block
+            const long long begin = (p.causal && p.layout == RA_LAYOUT_CONTIGUOUS) ? s * L : 0;
+            ra::launch_merge(run, run_lse, part, part_lse, (long long)p.B * p.H, p.S, begin, p.S - begin,
+                             p.d, sm, st);
+            count_launch();
+            if (cudaGetLastError() != cudaSuccess)
+                return RA_ERR_CUDA;
+        }
+        if (ring && (rs = rc.after_step(s, st)) != RA_OK)
+            return rs;
     }
+    if (ring && (rs = rc.end(st)) != RA_OK)
+        return rs;
     ra::launch_finalize(run, run_lse, out, lse, p.dtype == RA_DTYPE_BF16, (long long)p.rows(), p.S,
                         p.N, striped ? 1 : 0, p.d, sm, st);
     count_launch();
@@ -238,6 +396,44 @@ ra_status forward_alloc(const Problem &p, const void *q, const void *k, const vo
     if (ws && cudaFreeAsync(ws, st) != cudaSuccess && rs == RA_OK)
         rs = RA_ERR_CUDA;
     return rs;
+}
+
+// Workspace of ra_forward_ulysses: head-sharded q, k, v, out (input dtype)
+// and lse (fp32), each 256-byte aligned.
+struct UlyssesWs {
+    size_t q = 0, k = 0, v = 0, out = 0, lse = 0, total = 0;
+};
+
+// Validates the request; on success fills the per-device attention problem
+// (all devices' head groups as one batch of n_dev * B) and the workspace.
+ra_status ulysses_plan(int B, int H, int Hkv, int S, int d, int n_dev, int causal, int dtype, Problem *pa,
+                       UlyssesWs *w)
+{
+    if (n_dev < 1 || B < 1 || H < 1 || Hkv < 1 || S < 1)
+        return RA_ERR_INVALID_ARG;
+    if (S % n_dev != 0 || H % Hkv != 0)
+        return RA_ERR_INVALID_ARG;
+    // every device needs whole kv heads: the head count limits the devices
+    if (H % n_dev != 0 || Hkv % n_dev != 0)
+        return RA_ERR_UNSUPPORTED;
+    *pa = Problem{B * n_dev, H / n_dev, Hkv / n_dev, S, d, 1, RA_LAYOUT_CONTIGUOUS, causal, dtype,
+                  RA_MODE_FUSED};
+    ra_status rs = check_problem(*pa);
+    if (rs != RA_OK)
+        return rs;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += align256(bytes);
+        return at;
+    };
+    w->q = take(pa->q_elems() * pa->esz());
+    w->k = take(pa->kv_elems() * pa->esz());
+    w->v = take(pa->kv_elems() * pa->esz());
+    w->out = take(pa->q_elems() * pa->esz());
+    w->lse = take(pa->rows() * 4);
+    w->total = off;
+    return RA_OK;
 }
 
 }  // namespace
@@ -283,6 +479,114 @@ ra_status ra_forward_rank_major(const void *q, const void *k, const void *v, voi
     Problem p{B, H, Hkv, S, d, n_blocks, layout, causal, dtype, mode};
     p.rank_major = true;
     return forward_impl(p, q, k, v, out, lse, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+ra_status ra_forward_block(const void *q, const void *k, const void *v, float *out_s, float *lse_s, int B,
+                           int H, int Hkv, int S, int d, int n_blocks, int layout, int causal, int dtype,
+                           int rank, int step, ra_stream_t stream)
+{
+    const Problem p{B, H, Hkv, S, d, n_blocks, layout, causal, dtype, RA_MODE_PER_STEP};
+    ra_status rs = check_problem(p);
+    if (rs != RA_OK)
+        return rs;
+    if (rank < 0 || rank >= n_blocks || step < 0 || step >= n_blocks)
+        return RA_ERR_INVALID_ARG;
+    if (!q || !k || !v || !out_s || !lse_s)
+        return RA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out_s) || !aligned16(lse_s))
+        return RA_ERR_INVALID_ARG;
+    const size_t qb = p.q_elems() * p.esz(), kvb = p.kv_elems() * p.esz();
+    const size_t ob = p.q_elems() * 4, lb = p.rows() * 4;
+    for (const void *in : {q, k, v})
+        if (overlaps(out_s, ob, in, in == q ? qb : kvb) || overlaps(lse_s, lb, in, in == q ? qb : kvb))
+            return RA_ERR_INVALID_ARG;
+    if (overlaps(out_s, ob, lse_s, lb))
+        return RA_ERR_INVALID_ARG;
+    const int sm = sm_count_current();
+    cudaStream_t st = (cudaStream_t)stream;
+    const int j = ra_ring_block(rank, step, n_blocks);
+    if (ra_block_class(layout, causal, rank, j) == RA_CLS_SKIP) {
+        ra::launch_fill_empty(out_s, lse_s, (long long)B * H, S, (long long)rank * p.L(), p.L(), d, sm, st);
+        count_launch();
+        return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+    }
+    return attention_pass(p, q, k, v, out_s, lse_s, step, step + 1, true, sm, st, rank, rank + 1);
+}
+
+ra_status ra_all_to_all(const void *src, void *dst, int B, int Hn, int S, int d, int elem_bytes, int n_dev,
+                        int inverse, ra_stream_t stream)
+{
+    if (!src || !dst || B < 1 || Hn < 1 || S < 1 || d < 1 || n_dev < 1 || S % n_dev != 0 || Hn % n_dev != 0)
+        return RA_ERR_INVALID_ARG;
+    if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8)
+        return RA_ERR_INVALID_ARG;
+    if (inverse != 0 && inverse != 1)
+        return RA_ERR_INVALID_ARG;
+    if ((long long)B * Hn * S >= (1ll << 40))
+        return RA_ERR_UNSUPPORTED;
+    const long long row_bytes = (long long)d * elem_bytes;
+    const size_t total = (size_t)B * Hn * S * row_bytes;
+    if (overlaps(src, total, dst, total))
+        return RA_ERR_INVALID_ARG;
+    const uintptr_t mis = (reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst));
+    if ((row_bytes % 16 == 0 && (mis & 15u)) || (row_bytes % 4 == 0 && (mis & 3u)))
+        return RA_ERR_INVALID_ARG;
+    ra::launch_all_to_all(src, dst, B, Hn, S, n_dev, row_bytes, inverse, sm_count_current(),
+                          (cudaStream_t)stream);
+    count_launch();
+    return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+}
+
+
+size_t ra_ulysses_workspace_bytes(int B, int H, int Hkv, int S, int d, int n_dev, int causal, int dtype)
+{
+    Problem pa{};
+    UlyssesWs w;
+    return ulysses_plan(B, H, Hkv, S, d, n_dev, causal, dtype, &pa, &w) == RA_OK ? w.total : 0;
+}
+
+ra_status ra_forward_ulysses(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
+                             int Hkv, int S, int d, int n_dev, int causal, int dtype, void *ws, size_t ws_bytes,
+                             ra_stream_t stream)
+{
+    Problem pa{};
+    UlyssesWs w;
+    ra_status rs = ulysses_plan(B, H, Hkv, S, d, n_dev, causal, dtype, &pa, &w);
+    if (rs != RA_OK)
+        return rs;
+    if (!q || !k || !v || !out || !lse)
+        return RA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+        return RA_ERR_INVALID_ARG;
+    const size_t qb = pa.q_elems() * pa.esz(), kvb = pa.kv_elems() * pa.esz(), lb = pa.rows() * 4;
+    for (const void *in : {q, k, v})
+        if (overlaps(out, qb, in, in == q ? qb : kvb) || overlaps(lse, lb, in, in == q ? qb : kvb))
+            return RA_ERR_INVALID_ARG;
+    if (overlaps(out, qb, lse, lb))
+        return RA_ERR_INVALID_ARG;
+    if (!ws || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u))
+        return RA_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    const int sm = sm_count_current();
+    char *base = static_cast<char *>(ws);
+    const long long row = (long long)d * pa.esz();
+    // all-to-all in: every device gets all tokens of its heads
+    ra::launch_all_to_all(q, base + w.q, B, H, S, n_dev, row, 0, sm, st);
+    ra::launch_all_to_all(k, base + w.k, B, Hkv, S, n_dev, row, 0, sm, st);
+    ra::launch_all_to_all(v, base + w.v, B, Hkv, S, n_dev, row, 0, sm, st);
+    count_launch(3);
+    if (cudaGetLastError() != cudaSuccess)
+        return RA_ERR_CUDA;
+    // each device: exact attention over the whole sequence for its heads
+    rs = attention_pass(pa, base + w.q, base + w.k, base + w.v, base + w.out, (float *)(base + w.lse), 0, 1,
+                        dtype == RA_DTYPE_F32, sm, st);
+    if (rs != RA_OK)
+        return rs;
+    // all-to-all out: back to the sequence shards
+    ra::launch_all_to_all(base + w.out, out, B, H, S, n_dev, row, 1, sm, st);
+    ra::launch_all_to_all(base + w.lse, lse, B, H, S, n_dev, 4, 1, sm, st);
+    count_launch(2);
+    return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
 }
 
 unsigned long long ra_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
@@ -386,6 +690,24 @@ long long ra_schedule_units(int B, int H, int Hkv, int S, int n_blocks, int layo
         (!(s_begin == 0 && s_end == n_blocks) && s_end != s_begin + 1))
         return -1;
     const RaUnitSpace sp = ra_unit_space(B, H, Hkv, S, n_blocks, layout, causal, s_begin, s_end);
+    const long long n = ra_unit_count(sp);
+    for (long long u = 0; units && u < n && u < capacity; ++u) {
+        const RaUnit U = ra_unit_decode(sp, u);
+        int *o = units + 8 * u;
+        o[0] = U.bh0, o[1] = U.ta0, o[2] = U.bh1, o[3] = U.ta1;
+        o[4] = U.rank, o[5] = U.cost, o[6] = U.tile1_valid, o[7] = 0;
+    }
+    return n;
+}
+
+long long ra_schedule_block_units(int B, int H, int Hkv, int S, int n_blocks, int layout, int causal, int rank,
+                                  int step, int *units, long long capacity)
+{
+    const Problem p{B, H, Hkv, S, 64, n_blocks, layout, causal, RA_DTYPE_BF16, RA_MODE_PER_STEP};
+    if (check_problem(p) != RA_OK || rank < 0 || rank >= n_blocks || step < 0 || step >= n_blocks)
+        return -1;
+    const RaUnitSpace sp = ra_unit_space_ranks(
+        ra_unit_space(B, H, Hkv, S, n_blocks, layout, causal, step, step + 1), rank, rank + 1);
     const long long n = ra_unit_count(sp);
     for (long long u = 0; units && u < n && u < capacity; ++u) {
         const RaUnit U = ra_unit_decode(sp, u);
@@ -512,6 +834,7 @@ extern "C" ra_status ra_forward_noalloc(const void *q, const void *k, const void
     a.q = qk, a.k = kk, a.v = vk, a.out = ok_out, a.lse = ok_lse;
     a.B = B, a.H = H, a.Hkv = Hkv, a.S = S, a.d = d, a.N = n_blocks;
     a.layout = layout, a.causal = causal, a.s_begin = 0, a.s_end = n_blocks;
+    a.rank_lo = 0, a.rank_hi = n_blocks;
     a.out_f32 = 0;
     a.timeout_ns = g_timeout_ns;
     a.sm_count = sm;

@@ -43,7 +43,6 @@
 
 namespace ra {
 
-extern __device__ unsigned int g_ra_status;
 
 namespace {
 
@@ -88,6 +87,7 @@ struct PairParams {
     int n_units, H, Hkv, S, L, N, layout, causal, s_begin, s_end, out_f32, ntiles;
     float scale_log2;
     unsigned long long timeout_ns;
+    unsigned int *status;  // the library's device status word
 };
 
 struct Walk {
@@ -123,22 +123,24 @@ __device__ __forceinline__ int pair_unit_index(int round, int cluster, int G)
     return round * G + ((round & 1) ? (G - 1 - cluster) : cluster);
 }
 
-__device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, volatile int *abort, uint64_t tmo,
-                                      unsigned int site)
+// Waits record a timeout in the library's status word, whose device address
+// the launch passes in (`st`).
+__device__ __forceinline__ bool pwait(unsigned int *st, uint32_t bar, uint32_t parity, volatile int *abort,
+                                      uint64_t tmo, unsigned int site)
 {
-    return mbar_wait_cluster(bar, parity, abort, tmo, &g_ra_status, site);
+    return mbar_wait_cluster(bar, parity, abort, tmo, st, site);
 }
 
-__device__ __forceinline__ bool pwait_warp(uint32_t bar, uint32_t parity, volatile int *abort,
-                                           uint64_t tmo, unsigned int site)
+__device__ __forceinline__ bool pwait_warp(unsigned int *st, uint32_t bar, uint32_t parity,
+                                           volatile int *abort, uint64_t tmo, unsigned int site)
 {
-    return __all_sync(0xffffffffu, pwait(bar, parity, abort, tmo, site));
+    return __all_sync(0xffffffffu, pwait(st, bar, parity, abort, tmo, site));
 }
 
-__device__ __forceinline__ void pdrain(uint32_t bar, uint32_t parity, uint64_t tmo)
+__device__ __forceinline__ void pdrain(unsigned int *st, uint32_t bar, uint32_t parity, uint64_t tmo)
 {
     int never = 0;
-    mbar_wait_cluster(bar, parity, &never, tmo, &g_ra_status, PS_DRAIN);
+    mbar_wait_cluster(bar, parity, &never, tmo, st, PS_DRAIN);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
@@ -212,7 +214,7 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
                     break;
                 const RaUnit U = ra_unit_decode(p.sp, u);
                 // this CTA's query tile, once the previous unit's S MMAs are done
-                if (qcnt > 0 && !(ok = pwait(bar(ctrl->q_empty), (qcnt - 1) & 1, abort, tmo, PS_Q_EMPTY)))
+                if (qcnt > 0 && !(ok = pwait(p.status, bar(ctrl->q_empty), (qcnt - 1) & 1, abort, tmo, PS_Q_EMPTY)))
                     break;
                 if (leader)
                     mbar_arrive_expect_tx(bar(ctrl->q_full), 2 * Q_TILE);
@@ -230,7 +232,7 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
                 for (; w.valid(); w.advance()) {
                     const int row = kvbh * p.S + w.j * p.L + w.tb * RA_TILE;
                     const int ks = kcnt % KST;
-                    if (!(ok = pwait(bar(ctrl->k_empty[ks]), ((kcnt / KST) & 1) ^ 1, abort, tmo, PS_K_EMPTY)))
+                    if (!(ok = pwait(p.status, bar(ctrl->k_empty[ks]), ((kcnt / KST) & 1) ^ 1, abort, tmo, PS_K_EMPTY)))
                         break;
                     if (leader)
                         mbar_arrive_expect_tx(bar(ctrl->k_full[ks]), 2 * K_HALF);
@@ -241,7 +243,7 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
                                      lbar(ctrl->k_full[ks]), pol);
                     ++kcnt;
                     const int vs = vcnt % VST;
-                    if (!(ok = pwait(bar(ctrl->v_empty[vs]), ((vcnt / VST) & 1) ^ 1, abort, tmo, PS_V_EMPTY)))
+                    if (!(ok = pwait(p.status, bar(ctrl->v_empty[vs]), ((vcnt / VST) & 1) ^ 1, abort, tmo, PS_V_EMPTY)))
                         break;
                     if (leader)
                         mbar_arrive_expect_tx(bar(ctrl->v_full[vs]), 2 * V_HALF);
@@ -256,12 +258,12 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
                 for (int s = 0; s < KST; ++s) {
                     const uint32_t n = kcnt > (uint32_t)s ? (kcnt - s + KST - 1) / KST : 0;
                     if (n)
-                        pdrain(bar(ctrl->k_full[s]), (n - 1) & 1, tmo);
+                        pdrain(p.status, bar(ctrl->k_full[s]), (n - 1) & 1, tmo);
                 }
                 for (int s = 0; s < VST; ++s) {
                     const uint32_t n = vcnt > (uint32_t)s ? (vcnt - s + VST - 1) / VST : 0;
                     if (n)
-                        pdrain(bar(ctrl->v_full[s]), (n - 1) & 1, tmo);
+                        pdrain(p.status, bar(ctrl->v_full[s]), (n - 1) & 1, tmo);
                 }
             }
         }
@@ -296,13 +298,13 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
                     break;
                 const int n = ra_unit_decode(p.sp, u).cost;
                 // both CTAs' query tiles are in shared memory
-                if (!(ok = pwait(bar(ctrl->q_full), qcnt & 1, abort, tmo, PS_Q_FULL)))
+                if (!(ok = pwait(p.status, bar(ctrl->q_full), qcnt & 1, abort, tmo, PS_Q_FULL)))
                     break;
                 tc_fence_after();
                 const int pre = n < NSB ? n : NSB;
                 for (int jj = 0; jj < pre && ok; ++jj) {
                     const int ks = kcnt % KST;
-                    if (!(ok = pwait(bar(ctrl->k_full[ks]), (kcnt / KST) & 1, abort, tmo, PS_K_FULL)))
+                    if (!(ok = pwait(p.status, bar(ctrl->k_full[ks]), (kcnt / KST) & 1, abort, tmo, PS_K_FULL)))
                         break;
                     tc_fence_after();
                     issue_s(jj, ks);
@@ -313,15 +315,15 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
                 if (n <= NSB)
                     mma_commit_pair(bar(ctrl->q_empty));  // last S of the unit issued
                 // the previous unit's O has been read by both epilogues
-                if (ok && qcnt > 0 && !(ok = pwait(bar(ctrl->o_free), (qcnt - 1) & 1, abort, tmo, PS_O_FREE)))
+                if (ok && qcnt > 0 && !(ok = pwait(p.status, bar(ctrl->o_free), (qcnt - 1) & 1, abort, tmo, PS_O_FREE)))
                     break;
                 ++qcnt;
                 for (int j = 0; j < n && ok; ++j) {
                     const int buf = j % NSB;
                     const int vs = vcnt % VST;
-                    if (!(ok = pwait(bar(ctrl->v_full[vs]), (vcnt / VST) & 1, abort, tmo, PS_V_FULL)))
+                    if (!(ok = pwait(p.status, bar(ctrl->v_full[vs]), (vcnt / VST) & 1, abort, tmo, PS_V_FULL)))
                         break;
-                    if (!(ok = pwait(bar(ctrl->p_full[buf]), pcnt[buf] & 1, abort, tmo, PS_P_FULL)))
+                    if (!(ok = pwait(p.status, bar(ctrl->p_full[buf]), pcnt[buf] & 1, abort, tmo, PS_P_FULL)))
                         break;
                     ++pcnt[buf];
                     tc_fence_after();
@@ -333,7 +335,7 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
                         // S(j + NSB) reuses this buffer; the tensor pipe runs in
                         // issue order, so P(j) is read before it is overwritten
                         const int ks = kcnt % KST;
-                        if (!(ok = pwait(bar(ctrl->k_full[ks]), (kcnt / KST) & 1, abort, tmo, PS_K_FULL)))
+                        if (!(ok = pwait(p.status, bar(ctrl->k_full[ks]), (kcnt / KST) & 1, abort, tmo, PS_K_FULL)))
                             break;
                         tc_fence_after();
                         issue_s(buf, ks);
@@ -346,7 +348,7 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
                 }
             }
             mma_commit_pair(bar(ctrl->final_bar));
-            pdrain(bar(ctrl->final_bar), 0, tmo);
+            pdrain(p.status, bar(ctrl->final_bar), 0, tmo);
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax (both CTAs)
@@ -368,7 +370,7 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(bar(ctrl->xch[slot]));
-            if (!pwait_warp(bar(ctrl->xch[slot]), parity, abort, tmo, PS_XCH))
+            if (!pwait_warp(p.status, bar(ctrl->xch[slot]), parity, abort, tmo, PS_XCH))
                 return false;
             theirs = xb[(1 - h) * 128 + row];
             return true;
@@ -386,7 +388,7 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
             int jj = 0;
             for (; w.valid(); w.advance(), ++jj, ++gstep) {
                 const int buf = jj % NSB;
-                if (!(ok = pwait_warp(bar(ctrl->s_full[buf]), scnt[buf] & 1, abort, tmo, PS_S_FULL)))
+                if (!(ok = pwait_warp(p.status, bar(ctrl->s_full[buf]), scnt[buf] & 1, abort, tmo, PS_S_FULL)))
                     break;
                 ++scnt[buf];
                 tc_fence_after();
@@ -427,7 +429,7 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
                     // done: a parity wait is unambiguous.
                     const int pb = (jj - 1) % NSB;
                     const uint32_t idx = pvdone[pb] + (uint32_t)((jj - 1) / NSB);
-                    if (!(ok = pwait_warp(bar(ctrl->o_done[pb]), idx & 1, abort, tmo, PS_O_DONE)))
+                    if (!(ok = pwait_warp(p.status, bar(ctrl->o_done[pb]), idx & 1, abort, tmo, PS_O_DONE)))
                         break;
                     tc_fence_after();
 #pragma unroll 1
@@ -474,7 +476,7 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
             {
                 const int pb = (n - 1) % NSB;
                 const uint32_t idx = pvdone[pb] + (uint32_t)((n - 1) / NSB);
-                if (!(ok = pwait_warp(bar(ctrl->o_done[pb]), idx & 1, abort, tmo, PS_O_DONE)))
+                if (!(ok = pwait_warp(p.status, bar(ctrl->o_done[pb]), idx & 1, abort, tmo, PS_O_DONE)))
                     break;
             }
             for (int b2 = 0; b2 < NSB; ++b2)
@@ -590,7 +592,8 @@ cudaError_t launch_attn_pair(const TcLaunch &a, cudaStream_t st)
     if (!encode_box(&p.tm_q, a.q, (long long)a.B * a.H * a.S, RA_TILE) ||
         !encode_box(&p.tm_k, a.k, kv_rows, 64) || !encode_box(&p.tm_v, a.v, kv_rows, RA_TILE))
         return cudaErrorInvalidValue;
-    p.sp = ra_unit_space(a.B, a.H, a.Hkv, a.S, a.N, a.layout, a.causal, a.s_begin, a.s_end);
+    p.sp = ra_unit_space_ranks(ra_unit_space(a.B, a.H, a.Hkv, a.S, a.N, a.layout, a.causal, a.s_begin, a.s_end),
+                               a.rank_lo, a.rank_hi);
     const long long n_units = ra_unit_count(p.sp);
     if (n_units > 0x7fffffffll)
         return cudaErrorInvalidValue;
@@ -604,6 +607,9 @@ cudaError_t launch_attn_pair(const TcLaunch &a, cudaStream_t st)
     p.ntiles = (p.L + RA_TILE - 1) / RA_TILE;
     p.scale_log2 = 1.4426950408889634f / sqrtf((float)P_D);
     p.timeout_ns = a.timeout_ns;
+    p.status = device_status_ptr();
+    if (!p.status)
+        return cudaErrorInvalidValue;
     if (p.n_units <= 0)
         return cudaSuccess;
     const int clusters = p.n_units < a.sm_count / 2 ? p.n_units : a.sm_count / 2;

@@ -32,6 +32,7 @@
 // TMEM columns: S/P tile 0 [0,128), S/P tile 1 [128,256), O tile 0
 // [256,256+d), O tile 1 [384,384+d).
 #include <cstdint>
+#include <mutex>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -585,7 +586,8 @@ cudaError_t launch_d(const TcLaunch &a, cudaStream_t st)
         !encode_rows(&p.tm_k, a.k, (long long)a.B * a.Hkv * a.S, D) ||
         !encode_rows(&p.tm_v, a.v, (long long)a.B * a.Hkv * a.S, D))
         return cudaErrorInvalidValue;
-    p.sp = ra_unit_space(a.B, a.H, a.Hkv, a.S, a.N, a.layout, a.causal, a.s_begin, a.s_end);
+    p.sp = ra_unit_space_ranks(ra_unit_space(a.B, a.H, a.Hkv, a.S, a.N, a.layout, a.causal, a.s_begin, a.s_end),
+                               a.rank_lo, a.rank_hi);
     const long long n_units = ra_unit_count(p.sp);
     if (n_units > 0x7fffffffll)
         return cudaErrorInvalidValue;
@@ -633,6 +635,26 @@ cudaError_t launch_wait_probe(unsigned long long timeout_ns, cudaStream_t st)
 {
     ra_wait_probe_kernel<<<1, 1, 0, st>>>(timeout_ns);
     return cudaGetLastError();
+}
+
+unsigned int *device_status_ptr()
+{
+    constexpr int kMax = 64;
+    static std::mutex mu;
+    static unsigned int *ptr[kMax] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMax)
+        return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptr[dev]) {
+        void *a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_ra_status) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        ptr[dev] = static_cast<unsigned int *>(a);
+    }
+    return ptr[dev];
 }
 
 cudaError_t read_and_clear_device_status(unsigned int *status)

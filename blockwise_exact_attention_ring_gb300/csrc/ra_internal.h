@@ -15,7 +15,15 @@ constexpr unsigned int RA_DEV_TIMEOUT_CODE = 5;
 
 void launch_attn_f32(const float *q, const float *k, const float *v, float *out, float *lse,
                      int B, int H, int Hkv, int S, int d, int N, int layout, int causal,
-                     int s_begin, int s_end, cudaStream_t st);
+                     int s_begin, int s_end, int rank_lo, int rank_hi, cudaStream_t st);
+// Sequence-sharded [n][B][Hn][S/n][d] <-> head-sharded [n][B][Hn/n][S][d]
+// (inverse = 1 goes back); rows of row_bytes bytes, bit-exact.
+void launch_all_to_all(const void *src, void *dst, int B, int Hn, int S, int n_dev, long long row_bytes,
+                       int inverse, int sm_count, cudaStream_t st);
+// out[bh, row0 + r, :] = 0 and lse[bh, row0 + r] = -inf for r < nrows: the
+// partial of query rows that see no key at this step.
+void launch_fill_empty(float *out, float *lse, long long BH, int S, long long row0, long long nrows,
+                       int d, int sm_count, cudaStream_t st);
 
 void launch_permute(const void *src, void *dst, long long rows_total, int S, int N,
                     long long row_bytes, int inverse, int sm_count, cudaStream_t st);
@@ -37,10 +45,30 @@ struct TcLaunch {
     int B, H, Hkv, S, d, N;
     int layout, causal;
     int s_begin, s_end;          // ring steps walked by every unit
+    int rank_lo, rank_hi;        // query blocks (ranks) computed: [rank_lo, rank_hi)
     int out_f32;
     unsigned long long timeout_ns;
     int sm_count;
 };
+
+// Backward pass (bf16, d in {64, 128}): delta = rowsum(dout * out), then the
+// dK/dV and dQ tensor-core kernels.  All tensors in the layout's rank-major
+// order; lse and delta fp32 [B H S].
+struct BwdLaunch {
+    const void *q, *k, *v, *out, *dout;
+    const float *lse;
+    float *delta;                // written
+    void *dq, *dk, *dv;          // written, bf16
+    int B, H, Hkv, S, d, N;
+    int layout, causal;
+    unsigned long long timeout_ns;
+};
+cudaError_t launch_bwd(const BwdLaunch &a, cudaStream_t st);
+
+// Device address of the library's status word on the current device (the
+// word ra_check reads); kernels in other translation units get it as a
+// parameter.  nullptr if it cannot be looked up.
+unsigned int *device_status_ptr();
 
 // Returns cudaSuccess or the first CUDA error met while encoding tensor maps
 // or launching.

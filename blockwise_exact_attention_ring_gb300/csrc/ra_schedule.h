@@ -100,8 +100,10 @@ RA_HD int ra_unit_cost(int layout, int causal, int i, int ta_max, int ntiles, in
 // A unit is (column x, rank i, tile slot y): x runs over pairs of query heads
 // of one kv group (group size even: both heads share positions and masks) or
 // over single heads (odd group: the unit takes tiles 2y and 2y + 1 of one
-// head).  Ranks [i_lo, N) are active: all of them, except that at a single
-// contiguous causal ring step s only ranks i >= s hold a visible block.
+// head).  Ranks [i_lo, i_lo + n_act) are active: all of them, except that at
+// a single contiguous causal ring step s only ranks i >= s hold a visible
+// block, and a space restricted to some ranks (ra_unit_space_ranks) keeps
+// only those.
 // Order: x fastest; then, when the cost grows with the rank (contiguous
 // causal over all steps: cost = i ntiles + tiles of the diagonal block),
 // rank descending then tile descending, otherwise tile descending then rank
@@ -144,6 +146,18 @@ RA_HD RaUnitSpace ra_unit_space(int B, int H, int Hkv, int S, int n_blocks, int 
     return sp;
 }
 
+// The same space restricted to ranks [rank_lo, rank_hi): what one device of
+// the ring computes (rank_lo + 1 == rank_hi), in the same order and with the
+// same costs.
+RA_HD RaUnitSpace ra_unit_space_ranks(RaUnitSpace sp, int rank_lo, int rank_hi)
+{
+    const int lo = sp.i_lo > rank_lo ? sp.i_lo : rank_lo;
+    const int hi = sp.i_lo + sp.n_act < rank_hi ? sp.i_lo + sp.n_act : rank_hi;
+    sp.i_lo = lo;
+    sp.n_act = hi > lo ? hi - lo : 0;
+    return sp;
+}
+
 RA_HD long long ra_unit_count(const RaUnitSpace &sp)
 {
     return (long long)sp.X * sp.n_act * sp.Y;
@@ -167,12 +181,13 @@ RA_HD RaUnit ra_unit_decode(const RaUnitSpace &sp, long long u)
         r = u / sp.X;
     }
     int i, y;
+    const int i_top = sp.i_lo + sp.n_act - 1;  // highest active rank
     if (sp.rank_outer) {
-        i = sp.N - 1 - (int)(r / sp.Y);
+        i = i_top - (int)(r / sp.Y);
         y = sp.Y - 1 - (int)(r % sp.Y);
     } else {
         y = sp.Y - 1 - (int)(r / sp.n_act);
-        i = sp.N - 1 - (int)(r % sp.n_act);
+        i = i_top - (int)(r % sp.n_act);
     }
     RaUnit U;
     if (sp.head_pairs) {

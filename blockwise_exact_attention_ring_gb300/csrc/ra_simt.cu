@@ -1,6 +1,7 @@
 // SIMT kernels of the ring-attention library:
 //   * ra_attn_f32_kernel  exact fp32 ring-ordered attention (no tensor cores)
 //   * ra_permute_kernel   natural <-> striped token order, bit-exact copy
+//   * ra_all_to_all_kernel sequence-sharded <-> head-sharded relayout (Ulysses)
 //   * ra_merge_kernel     running-softmax merge of one ring step's partials
 //   * ra_finalize_kernel  fp32 running result -> output dtype, natural order
 #include <cstdint>
@@ -26,11 +27,11 @@ __global__ void __launch_bounds__(F32_WARPS * 32)
 ra_attn_f32_kernel(const float *__restrict__ q, const float *__restrict__ k,
                    const float *__restrict__ v, float *__restrict__ out,
                    float *__restrict__ lse, int H, int Hkv, int S, int d, int L, int N,
-                   int layout, int causal, int s_begin, int s_end, float scale)
+                   int layout, int causal, int s_begin, int s_end, int rank_lo, float scale)
 {
     const int lane = threadIdx.x & 31;
     const int a = blockIdx.x * F32_WARPS + (threadIdx.x >> 5);
-    const int i = blockIdx.y;
+    const int i = rank_lo + (int)blockIdx.y;
     const long long bh = blockIdx.z;
     if (a >= L)
         return;
@@ -94,13 +95,44 @@ ra_attn_f32_kernel(const float *__restrict__ q, const float *__restrict__ k,
 
 void launch_attn_f32(const float *q, const float *k, const float *v, float *out, float *lse,
                      int B, int H, int Hkv, int S, int d, int N, int layout, int causal,
-                     int s_begin, int s_end, cudaStream_t st)
+                     int s_begin, int s_end, int rank_lo, int rank_hi, cudaStream_t st)
 {
     const int L = S / N;
-    dim3 grid((L + F32_WARPS - 1) / F32_WARPS, N, B * H);
+    if (rank_hi <= rank_lo)
+        return;
+    dim3 grid((L + F32_WARPS - 1) / F32_WARPS, rank_hi - rank_lo, B * H);
     ra_attn_f32_kernel<<<grid, F32_WARPS * 32, 0, st>>>(
-        q, k, v, out, lse, H, Hkv, S, d, L, N, layout, causal, s_begin, s_end,
+        q, k, v, out, lse, H, Hkv, S, d, L, N, layout, causal, s_begin, s_end, rank_lo,
         1.0f / sqrtf((float)d));
+}
+
+// ---------------------------------------------------------------- empty rows
+// A partial over no visible key: O = 0 and lse = -inf, the neutral element of
+// the merge.  One thread per 16-byte word of out (d % 4 == 0) or per float.
+__global__ void ra_fill_empty_kernel(float *__restrict__ out, float *__restrict__ lse, long long BH,
+                                     int S, long long row0, long long nrows, int d)
+{
+    const long long words = (long long)d / 4;
+    const long long total = BH * nrows * words;
+    for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < total;
+         x += (long long)gridDim.x * blockDim.x) {
+        const long long w = x % words, rr = x / words;
+        const long long row = (rr / nrows) * S + row0 + rr % nrows;
+        reinterpret_cast<float4 *>(out + row * d)[w] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (w == 0)
+            lse[row] = -INFINITY;
+    }
+}
+
+void launch_fill_empty(float *out, float *lse, long long BH, int S, long long row0, long long nrows,
+                       int d, int sm_count, cudaStream_t st)
+{
+    const long long total = BH * nrows * (d / 4);
+    if (total <= 0)
+        return;
+    const long long want = (total + 255) / 256;
+    const int grid = (int)(want < 8ll * sm_count ? want : 8ll * sm_count);
+    ra_fill_empty_kernel<<<grid, 256, 0, st>>>(out, lse, BH, S, row0, nrows, d);
 }
 
 // ---------------------------------------------------------------- permute
@@ -163,6 +195,91 @@ void launch_permute(const void *src, void *dst, long long rows_total, int S, int
         const int wpr = (int)row_bytes;
         ra_permute_kernel<uint8_t, 4><<<grid_for(rows_total * wpr), threads, 0, st>>>(
             (const uint8_t *)src, (uint8_t *)dst, rows_total, S, L, N, wpr, inverse);
+    }
+}
+
+// ---------------------------------------------------------------- all-to-all
+// Sequence-sharded <-> head-sharded relayout of DeepSpeed Ulysses, the
+// alternative to the ring that the "Ring Attention" page names (section on
+// other kinds of parallelism: an all-to-all exchange gives every device all
+// tokens of a subset of the heads).  n devices, Hn heads, Hg = Hn / n per
+// device, L = S / n tokens per device:
+//   sequence-sharded  [n][B][Hn][L][d]  device i holds tokens [i L, i L + L)
+//   head-sharded      [n][B][Hg][S][d]  device g holds heads [g Hg, g Hg + Hg)
+// The grid walks destination rows (coalesced writes); each source row is read
+// whole, UNROLL loads in flight per thread as in the permutation.
+template <typename VEC, int UNROLL>
+__global__ void ra_all_to_all_kernel(const VEC *__restrict__ src, VEC *__restrict__ dst, long long n_rows_total,
+                                     int B, int Hn, int Hg, int S, int L, int words_per_row, int inverse)
+{
+    const long long n = n_rows_total * words_per_row;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long base = blockIdx.x * (long long)blockDim.x + threadIdx.x; base < n;
+         base += stride * UNROLL) {
+        VEC v[UNROLL];
+        long long at[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const long long idx = base + u * stride;
+            at[u] = idx;
+            if (idx < n) {
+                const long long row = idx / words_per_row;
+                const int w = (int)(idx - row * words_per_row);
+                long long from;
+                if (!inverse) {
+                    // dst row ((g B + b) Hg + h') S + t  <-  src ((i B + b) Hn + g Hg + h') L + a
+                    const int t = (int)(row % S);
+                    const long long r1 = row / S;
+                    const int hl = (int)(r1 % Hg);
+                    const long long r2 = r1 / Hg;
+                    const int b = (int)(r2 % B);
+                    const int g = (int)(r2 / B);
+                    const int i = t / L, a = t - i * L;
+                    from = (((long long)i * B + b) * Hn + (long long)g * Hg + hl) * L + a;
+                } else {
+                    // dst row ((i B + b) Hn + h) L + a  <-  src ((g B + b) Hg + h') S + i L + a
+                    const int a = (int)(row % L);
+                    const long long r1 = row / L;
+                    const int h = (int)(r1 % Hn);
+                    const long long r2 = r1 / Hn;
+                    const int b = (int)(r2 % B);
+                    const int i = (int)(r2 / B);
+                    const int g = h / Hg, hl = h - g * Hg;
+                    from = (((long long)g * B + b) * Hg + hl) * S + (long long)i * L + a;
+                }
+                v[u] = src[from * words_per_row + w];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u)
+            if (at[u] < n)
+                dst[at[u]] = v[u];
+    }
+}
+
+void launch_all_to_all(const void *src, void *dst, int B, int Hn, int S, int n_dev, long long row_bytes,
+                       int inverse, int sm_count, cudaStream_t st)
+{
+    const long long rows_total = (long long)B * Hn * S;
+    const int L = S / n_dev, Hg = Hn / n_dev;
+    const int threads = 256;
+    auto grid_for = [&](long long n) {
+        long long g = (n + threads - 1) / threads;
+        const long long cap = (long long)sm_count * 8;
+        return (int)(g < cap ? (g > 0 ? g : 1) : cap);
+    };
+    if (row_bytes % 16 == 0) {
+        const int wpr = (int)(row_bytes / 16);
+        ra_all_to_all_kernel<uint4, 4><<<grid_for(rows_total * wpr), threads, 0, st>>>(
+            (const uint4 *)src, (uint4 *)dst, rows_total, B, Hn, Hg, S, L, wpr, inverse);
+    } else if (row_bytes % 4 == 0) {
+        const int wpr = (int)(row_bytes / 4);
+        ra_all_to_all_kernel<uint32_t, 4><<<grid_for(rows_total * wpr), threads, 0, st>>>(
+            (const uint32_t *)src, (uint32_t *)dst, rows_total, B, Hn, Hg, S, L, wpr, inverse);
+    } else {
+        const int wpr = (int)row_bytes;
+        ra_all_to_all_kernel<uint8_t, 4><<<grid_for(rows_total * wpr), threads, 0, st>>>(
+            (const uint8_t *)src, (uint8_t *)dst, rows_total, B, Hn, Hg, S, L, wpr, inverse);
     }
 }
 

@@ -76,8 +76,17 @@ typedef enum { RA_LAYOUT_CONTIGUOUS = 0, RA_LAYOUT_STRIPED = 1 } ra_layout;
  *   blocks in ring order and keeps the running softmax on chip.
  * RA_MODE_PER_STEP: one launch per ring step s writes that step's partial
  *   (out_s, lse_s) for every rank, then ra_merge-style merging folds it into
- *   the running result, as each ring device would after receiving a block. */
-typedef enum { RA_MODE_FUSED = 0, RA_MODE_PER_STEP = 1 } ra_mode;
+ *   the running result, as each ring device would after receiving a block.
+ * RA_MODE_RING: RA_MODE_PER_STEP with the key/value rotation made explicit:
+ *   before step s every rank's block is copied (by the copy engine, on a
+ *   second stream of the library's own) from where the previous rank held it
+ *   into a double-buffered workspace copy, and step s reads that copy.  The
+ *   copy for step s + 1 overlaps the compute of step s, as the send of the
+ *   block to the next device overlaps the block computation on a real ring
+ *   ("Ring Attention" page, section "Halka Dikkati Nasil Calisir": each device
+ *   passes its key/value block to the next one while it computes).  Same
+ *   result as RA_MODE_PER_STEP, bit for bit. */
+typedef enum { RA_MODE_FUSED = 0, RA_MODE_PER_STEP = 1, RA_MODE_RING = 2 } ra_mode;
 
 typedef enum { RA_DTYPE_BF16 = 0, RA_DTYPE_F32 = 1 } ra_dtype;
 
@@ -111,7 +120,8 @@ ra_status ra_forward_f32(const float *q, const float *k, const float *v, float *
 /*
  * ra_workspace_bytes - bytes of scratch ra_forward_ws needs for this problem
  * (striped copies of q, k, v, out and lse; per-step running and partial
- * results).  0 when none is needed (bf16 contiguous fused).
+ * results; for RA_MODE_RING two rotating copies of k and v).  0 when none is
+ * needed (bf16 contiguous fused).
  * dtype is a ra_dtype, mode a ra_mode.  Returns 0 for an invalid request.
  */
 size_t ra_workspace_bytes(int B, int H, int Hkv, int S, int d, int n_blocks, int layout,
@@ -139,13 +149,89 @@ ra_status ra_forward_ws(const void *q, const void *k, const void *v, void *out, 
  * use that order and no permutation is launched, as for a model that keeps
  * its activations striped from embedding to output.  Same arguments, types
  * and error rules as ra_forward_ws; the workspace is needed only for
- * RA_MODE_PER_STEP (ra_workspace_bytes of the contiguous layout).
+ * RA_MODE_PER_STEP and RA_MODE_RING (ra_workspace_bytes of the contiguous
+ * layout).
  * Source: "Ring Attention" page, section "Halka Dikkati Nasil Calisir".
  */
 ra_status ra_forward_rank_major(const void *q, const void *k, const void *v, void *out,
                                 float *lse, int B, int H, int Hkv, int S, int d, int n_blocks,
                                 int layout, int causal, int dtype, int mode, void *ws,
                                 size_t ws_bytes, ra_stream_t stream);
+
+/*
+ * ra_forward_block - the work of one device of the ring at one ring step:
+ * the partial attention of query block `rank` against key/value block
+ * j = (rank - step) mod n_blocks, the block that device holds after `step`
+ * rotations ("Ring Attention" page, section "Halka Dikkati Nasil Calisir":
+ * each device computes attention for its local query block against the key
+ * and value block it currently holds, then passes that block on).
+ *   q, k, v   device tensors in the layout's rank-major order (as for
+ *             ra_forward_rank_major), dtype RA_DTYPE_BF16 or RA_DTYPE_F32;
+ *   out_s     fp32 [B,H,S,d], lse_s fp32 [B,H,S] (natural log): only the rows
+ *             of block `rank` (rows rank*L .. rank*L + L - 1 of every head)
+ *             are written, with the partial normalised by its own sum; rows
+ *             that see no key at this step get out 0 and lse -inf (the whole
+ *             block when it is masked, e.g. contiguous causal with step > rank).
+ * Merging the n_blocks partials of a rank with ra_merge, in any order, gives
+ * its rows of ra_forward's result (up to rounding).  Caller-owned buffers,
+ * 16-byte aligned; no allocation; asynchronous on `stream`.  Errors:
+ * RA_ERR_INVALID_ARG (bad sizes, rank or step outside [0, n_blocks), null,
+ * misaligned or overlapping buffers), RA_ERR_UNSUPPORTED (d % 4 != 0, or a
+ * bf16 head dimension other than 64 / 128), RA_ERR_CUDA.  Nothing is launched
+ * on an error.
+ */
+ra_status ra_forward_block(const void *q, const void *k, const void *v, float *out_s,
+                           float *lse_s, int B, int H, int Hkv, int S, int d, int n_blocks,
+                           int layout, int causal, int dtype, int rank, int step,
+                           ra_stream_t stream);
+
+/*
+ * ra_all_to_all - the all-to-all exchange of DeepSpeed Ulysses, the
+ * alternative to the ring named on the "Ring Attention" page (section on
+ * ring attention and other kinds of parallelism: every device receives all
+ * tokens of a subset of the attention heads), emulated as one relayout of
+ * device-major buffers.  With L = S / n_dev and Hg = Hn / n_dev:
+ *   sequence-sharded [n_dev][B][Hn][L][d]: device i holds tokens [iL, iL+L)
+ *     of every head;
+ *   head-sharded     [n_dev][B][Hg][S][d]: device g holds all tokens of
+ *     heads [g Hg, g Hg + Hg).
+ * inverse = 0 maps sequence-sharded src to head-sharded dst, 1 the reverse.
+ * Rows of d elements of elem_bytes bytes (1, 2, 4 or 8) are copied bit-exact.
+ * Device pointers, caller-owned, not overlapping; 16-byte aligned when
+ * d * elem_bytes % 16 == 0, else 4-byte aligned when it is a multiple of 4.
+ * Errors: RA_ERR_INVALID_ARG (sizes, S % n_dev, Hn % n_dev, alignment,
+ * overlap), RA_ERR_CUDA.  Asynchronous on `stream`.
+ */
+ra_status ra_all_to_all(const void *src, void *dst, int B, int Hn, int S, int d,
+                        int elem_bytes, int n_dev, int inverse, ra_stream_t stream);
+
+/*
+ * ra_ulysses_workspace_bytes - scratch ra_forward_ulysses needs (head-sharded
+ * q, k, v and out in the input dtype, lse fp32); 0 for an invalid or
+ * unsupported request.
+ */
+size_t ra_ulysses_workspace_bytes(int B, int H, int Hkv, int S, int d, int n_dev,
+                                  int causal, int dtype);
+
+/*
+ * ra_forward_ulysses - exact attention over n_dev emulated devices the
+ * Ulysses way: all-to-all q, k, v from sequence shards to head shards,
+ * attention of every device over the whole sequence for its heads (causal
+ * mask on natural positions), all-to-all out and lse back.
+ *   q [n_dev][B][H][L][d], k, v [n_dev][B][Hkv][L][d]: sequence shards
+ *     (device i holds tokens [iL, iL + L)), dtype RA_DTYPE_BF16 or F32;
+ *   out (q's shape and dtype), lse fp32 [n_dev][B][H][L], natural log.
+ * The result equals ra_forward's on the same tokens (the shards laid side by
+ * side).  Requires H % n_dev == 0 and Hkv % n_dev == 0 (a device holds whole
+ * kv heads, so the kv head count bounds the devices): RA_ERR_UNSUPPORTED
+ * otherwise; the tensor-core path needs d in {64, 128}.  ws: device scratch
+ * of ra_ulysses_workspace_bytes bytes, 256-byte aligned (RA_ERR_WORKSPACE).
+ * Other errors as ra_forward.  Asynchronous on `stream`; no allocation.
+ */
+ra_status ra_forward_ulysses(const void *q, const void *k, const void *v, void *out,
+                             float *lse, int B, int H, int Hkv, int S, int d, int n_dev,
+                             int causal, int dtype, void *ws, size_t ws_bytes,
+                             ra_stream_t stream);
 
 /*
  * ra_forward_noalloc - ra_forward for callers that cannot allocate device
@@ -284,6 +370,16 @@ long long ra_schedule_stats(int layout, int causal, int n_blocks, int L,
  */
 long long ra_schedule_units(int B, int H, int Hkv, int S, int n_blocks, int layout, int causal,
                             int s_begin, int s_end, int *units, long long capacity);
+
+/*
+ * ra_schedule_block_units - host-only view of the units ra_forward_block
+ * launches for (rank, step): the same enumeration and record format as
+ * ra_schedule_units, restricted to query block `rank` at ring step `step`.
+ * Returns the count (0 when the block is fully masked), or -1 on bad input.
+ * Source: as for ra_schedule_stats.
+ */
+long long ra_schedule_block_units(int B, int H, int Hkv, int S, int n_blocks, int layout, int causal,
+                                  int rank, int step, int *units, long long capacity);
 
 #ifdef __cplusplus
 }

@@ -12,6 +12,10 @@ Contents
 ``merge``          the definition of combining two partial softmax results.
 ``stripe_order``   the striped token layout as a plain index map.
 ``permute``        apply that index map to the sequence axis (numpy indexing).
+``shard_sequence`` / ``gather_sequence``  natural [B, Hn, S, d] <-> the
+                   sequence shards of n devices [n, B, Hn, S/n, d].
+``heads_of``       what each device holds after the Ulysses all-to-all: all
+                   tokens of its heads, [n, B, Hn/n, S, d].
 
 Sources (web pages on ring attention):
   * "Ring Attention" glossary page (ultralytics.com/tr), section
@@ -19,6 +23,9 @@ Sources (web pages on ring attention):
     ring, the running sums of exponentiated scores and weighted values that are
     divided at the end, and striped attention, which hands every device tokens
     spread evenly along the sequence.
+  * "Ring Attention" page, section on ring attention and other kinds of
+    parallelism: DeepSpeed Ulysses, where an all-to-all exchange gives every
+    device all tokens of a subset of the attention heads.
   * "Context Parallelism" glossary page (ultralytics.com/tr), section
     "Pratik Kullanim ve Odunlesimler": [batch, heads, sequence, dim] layout,
     sequence on dim 2, causal scaled-dot-product attention.
@@ -204,6 +211,37 @@ def permute(x: np.ndarray, n_blocks: int, inverse: bool = False, seq_dim: int = 
     inv = np.empty_like(order)
     inv[order] = np.arange(order.size, dtype=np.int64)
     return np.take(x, inv, axis=seq_dim)
+
+
+def shard_sequence(x: np.ndarray, n_dev: int) -> np.ndarray:
+    """Split the sequence axis (dim 2) of x [B, Hn, S, ...] into n_dev
+    consecutive blocks and stack them in front: out[i] = x[:, :, iL:(i+1)L]."""
+    x = np.asarray(x)
+    S = x.shape[2]
+    if n_dev < 1 or S % n_dev != 0:
+        raise ValueError("S must be a multiple of n_dev")
+    L = S // n_dev
+    return np.stack([x[:, :, i * L:(i + 1) * L] for i in range(n_dev)])
+
+
+def gather_sequence(shards: np.ndarray) -> np.ndarray:
+    """Inverse of shard_sequence: concatenate the device blocks along the
+    sequence axis."""
+    shards = np.asarray(shards)
+    return np.concatenate(list(shards), axis=2)
+
+
+def heads_of(shards: np.ndarray) -> np.ndarray:
+    """After the Ulysses all-to-all, device g holds every token of heads
+    [g Hg, (g + 1) Hg), Hg = Hn / n: out[g] = full[:, g Hg:(g + 1) Hg] of the
+    sequence put back together from the shards [n, B, Hn, L, ...]."""
+    shards = np.asarray(shards)
+    n, Hn = shards.shape[0], shards.shape[2]
+    if Hn % n != 0:
+        raise ValueError("the head count must be a multiple of the device count")
+    full = gather_sequence(shards)
+    Hg = Hn // n
+    return np.stack([full[:, g * Hg:(g + 1) * Hg] for g in range(n)])
 
 
 if __name__ == "__main__":  # pragma: no cover - manual build helper

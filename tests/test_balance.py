@@ -1,0 +1,85 @@
+"""Per-device ring steps on the host: the units ra_forward_block launches and
+the lock-step critical-path model of the ring's load balance."""
+import itertools
+
+import numpy as np
+import pytest
+
+import blockwise_exact_attention_ring_gb300 as ra
+from blockwise_exact_attention_ring_gb300 import balance
+
+
+@pytest.mark.parametrize("B,H,Hkv,S,N", [(1, 4, 2, 1024, 4), (2, 3, 1, 1536, 3), (1, 2, 2, 640, 5),
+                                         (1, 32, 8, 262144, 8)])
+@pytest.mark.parametrize("layout,causal", [("contiguous", True), ("striped", True),
+                                           ("contiguous", False), ("striped", False)])
+def test_block_units_are_one_ranks_share_of_the_step(B, H, Hkv, S, N, layout, causal):
+    """ra_forward_block(rank, step) launches exactly the units of ring step
+    `step` that belong to query block `rank`, in the same heaviest-first order."""
+    for s in range(N):
+        step_units = ra.schedule_units(B, H, Hkv, S, N, layout, causal, s)
+        seen = 0
+        for i in range(N):
+            got = ra.block_units(B, H, Hkv, S, N, layout, causal, i, s)
+            want = step_units[step_units[:, 4] == i]
+            assert np.array_equal(got, want), (s, i)
+            assert np.all(got[:, 4] == i)
+            seen += len(got)
+        assert seen == len(step_units)
+
+
+def test_block_units_empty_for_masked_block():
+    """Contiguous causal: query block i sees nothing of block j > i, which it
+    holds at steps s > i."""
+    N = 4
+    for i, s in itertools.product(range(N), range(N)):
+        n = len(ra.block_units(1, 2, 1, 1024, N, "contiguous", True, i, s))
+        assert (n == 0) == (s > i)
+
+
+def test_block_units_rejects_bad_rank_or_step():
+    L = ra.lib()
+    for rank, step in [(-1, 0), (4, 0), (0, -1), (0, 4)]:
+        assert L.ra_schedule_block_units(1, 2, 1, 1024, 4, 0, 1, rank, step, None, 0) == -1
+
+
+@pytest.mark.parametrize("N,L", [(1, 7), (2, 128), (4, 1000), (8, 32768), (32, 32768)])
+def test_critical_path_closed_forms(N, L):
+    """Visible pairs per (device, step), summed over the slowest device of
+    each step.  Contiguous causal: step 0 is the diagonal block L(L+1)/2,
+    every later step has a device with a full block L^2.  Striped causal:
+    every step has a device on an inclusive diagonal block, L(L+1)/2.
+    Non-causal: L^2 everywhere, no imbalance."""
+    S = N * L
+    total = S * (S + 1) / 2
+    c = balance.model("contiguous", True, N, L)
+    s = balance.model("striped", True, N, L)
+    f = balance.model("striped", False, N, L)
+    assert c["total"] == total and s["total"] == total
+    assert c["critical_path"] == L * (L + 1) / 2 + (N - 1) * L * L
+    assert s["critical_path"] == N * L * (L + 1) / 2
+    assert c["ideal"] == pytest.approx(total / N)
+    assert f["critical_path"] == N * L * L and f["imbalance"] == 1.0
+    assert c["imbalance"] == pytest.approx(c["critical_path"] / (total / N))
+    # striping never loses, and gains ~ (2N - 1) / N for large blocks
+    assert s["critical_path"] <= c["critical_path"]
+    if N > 1 and L >= 1000:
+        assert c["critical_path"] / s["critical_path"] == pytest.approx((2 * N - 1) / N, rel=2e-3)
+
+
+def test_tile_model_counts_masked_half_of_diagonal_tiles():
+    """In tiles, a diagonal block of T tiles costs T(T+1)/2 launched tiles
+    (the masked upper half of each diagonal tile still runs)."""
+    N, L = 4, 512
+    T = L // 128
+    c = balance.model("contiguous", True, N, L, unit="tiles")
+    assert c["step_max"][0] == T * (T + 1) / 2
+    assert all(m == T * T for m in c["step_max"][1:])
+
+
+def test_measured_summary_matches_model_on_model_input():
+    _, pairs, _ = ra.schedule_stats("contiguous", True, 8, 256)
+    assert balance.measured(pairs)["critical_path"] == balance.model("contiguous", True, 8, 256)[
+        "critical_path"]
+    with pytest.raises(ValueError):
+        balance.summarize(np.zeros((2, 3)))

@@ -47,7 +47,7 @@ def _check(out, lse, q, k, v, causal, rows=None):
 # ---------------------------------------------------------------- fp32 path
 
 @pytest.mark.parametrize("layout,mode", list(itertools.product(["contiguous", "striped"],
-                                                                ["fused", "per_step"])))
+                                                                ["fused", "per_step", "ring"])))
 def test_page_example_fp32(layout, mode):
     """The pages' 4-device, block-8, dim-16 simulation on the seed-0 inputs."""
     q, k, v = _dev(*inputs.page_example_qkv())
@@ -89,13 +89,27 @@ BF16_SHAPES = [
 @pytest.mark.parametrize("shape", BF16_SHAPES)
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("layout", ["contiguous", "striped"])
-@pytest.mark.parametrize("mode", ["fused", "per_step"])
+@pytest.mark.parametrize("mode", ["fused", "per_step", "ring"])
 def test_bf16_small(shape, causal, layout, mode):
     B, H, Hkv, S, d, N = shape
     q, k, v = _dev(*inputs.make_qkv(B, H, Hkv, S, d, seed=7 * S + d + N))
     out, lse = ra.forward(q, k, v, n_blocks=N, layout=layout, causal=causal, mode=mode)
     ra.check()
     _check(out, lse, q, k, v, causal)
+
+
+@pytest.mark.parametrize("layout,causal,N", [("striped", True, 4), ("contiguous", True, 5),
+                                             ("contiguous", False, 2), ("striped", True, 1)])
+def test_ring_rotation_is_bitwise_per_step(layout, causal, N):
+    """RA_MODE_RING reads every step's key/value blocks from the copies the
+    copy stream rotated into place; the kernels and their order are those of
+    the per-step mode, so the results are identical bit for bit."""
+    q, k, v = _dev(*inputs.make_qkv(1, 4, 2, 640 * N, 128, seed=50 + N))
+    a = ra.forward(q, k, v, n_blocks=N, layout=layout, causal=causal, mode="per_step")
+    b = ra.forward(q, k, v, n_blocks=N, layout=layout, causal=causal, mode="ring")
+    ra.check()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    _check(b[0], b[1], q, k, v, causal)
 
 
 def test_bf16_result_independent_of_ring_size():

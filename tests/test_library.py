@@ -79,7 +79,12 @@ def test_workspace_sizes():
     assert striped == 2 * (B * H * S * d) * 2 + 2 * (B * Hkv * S * d) * 2 + B * H * S * 4
     per_step = ra.workspace_bytes(B, H, Hkv, S, d, N, "contiguous", True, "per_step")
     assert per_step == 2 * (B * H * S * d * 4 + B * H * S * 4)
+    ring = ra.workspace_bytes(B, H, Hkv, S, d, N, "contiguous", True, "ring")
+    # plus two rotating copies of k and v (bf16)
+    assert ring == per_step + 4 * (B * Hkv * S * d) * 2
+    assert ra.workspace_bytes(B, H, Hkv, S, d, 1, "contiguous", True, "ring") == per_step
     assert ra.workspace_bytes(B, 3, 2, S, d, N) == 0  # invalid request -> 0
+    assert ra.lib().ra_workspace_bytes(B, H, Hkv, S, d, N, 0, 1, 3, 0) == 0  # unknown mode
 
 
 def test_permute_and_merge_validation():
@@ -100,3 +105,44 @@ def test_every_declared_function_has_ctypes_signature():
         if n in ("ra_version", "ra_launch_count"):
             continue
         assert f.argtypes is not None, n
+
+
+def _header_param_counts():
+    import re
+    with open(rb.HEADER) as fh:
+        text = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
+    counts = {}
+    for m in re.finditer(r"\b(ra_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", text):
+        params = m.group(2).strip()
+        counts[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return counts
+
+
+def test_ctypes_signatures_match_header_arity():
+    """A wrong argument count shifts every later argument; check each binding
+    against the number of parameters the header declares."""
+    L = ra.lib()
+    counts = _header_param_counts()
+    assert set(counts) == set(rb.header_functions())
+    for n, c in counts.items():
+        f = getattr(L, n)
+        got = len(f.argtypes) if f.argtypes is not None else 0
+        assert got == c, (n, got, c)
+
+
+def test_ulysses_validation_without_gpu():
+    """Requests the library rejects before touching the GPU."""
+    L = ra.lib()
+    # Hkv = 2 cannot be split over 4 devices
+    assert L.ra_ulysses_workspace_bytes(1, 8, 2, 1024, 128, 4, 1, 0) == 0
+    assert L.ra_forward_ulysses(Q, K, V, OUT, LSE, 1, 8, 2, 1024, 128, 4, 1, 0, None, 0, None) == \
+        rb.RA_ERR_UNSUPPORTED
+    # S % n_dev
+    assert L.ra_forward_ulysses(Q, K, V, OUT, LSE, 1, 8, 8, 1000, 128, 3, 1, 0, None, 0, None) == \
+        rb.RA_ERR_INVALID_ARG
+    # a valid request without workspace
+    need = L.ra_ulysses_workspace_bytes(1, 8, 4, 1024, 128, 4, 1, 0)
+    assert need == 2 * (8 * 1024 * 128 * 2) + 2 * (4 * 1024 * 128 * 2) + 8 * 1024 * 4
+    assert L.ra_forward_ulysses(Q, K, V, OUT, LSE, 1, 8, 4, 1024, 128, 4, 1, 0, None, 0, None) == \
+        rb.RA_ERR_WORKSPACE
+    assert L.ra_all_to_all(Q, K, 1, 6, 32, 8, 2, 4, 0, None) == rb.RA_ERR_INVALID_ARG   # Hn % n

@@ -307,6 +307,29 @@ def test_stripe_order_definition(S, N):
     assert np.array_equal(oracle.permute(y, N, inverse=True), x)
 
 
+@pytest.mark.parametrize("B,Hn,S,n", [(1, 4, 8, 2), (2, 6, 12, 3), (1, 8, 16, 8), (2, 2, 6, 1)])
+def test_ulysses_relayout_definition(B, Hn, S, n):
+    """Brute force over every element: after the all-to-all, device g's local
+    head h' at token t is head g Hg + h' of the device that held token t
+    (device t // L, local row t % L)."""
+    L, Hg = S // n, Hn // n
+    x = np.arange(B * Hn * S * 3).reshape(B, Hn, S, 3)
+    shards = oracle.shard_sequence(x, n)
+    assert shards.shape == (n, B, Hn, L, 3)
+    heads = oracle.heads_of(shards)
+    assert heads.shape == (n, B, Hg, S, 3)
+    for g in range(n):
+        for b in range(B):
+            for hl in range(Hg):
+                for t in range(S):
+                    assert np.array_equal(heads[g, b, hl, t], shards[t // L, b, g * Hg + hl, t % L])
+    assert np.array_equal(oracle.gather_sequence(shards), x)
+    # every element moved exactly once
+    assert sorted(heads.reshape(-1).tolist()) == list(range(x.size))
+    with pytest.raises(ValueError):
+        oracle.shard_sequence(x, S + 1)
+
+
 def test_oracle_rejects_bad_arguments():
     q = torch.zeros(1, 3, 4, 2, dtype=torch.float64)
     k = torch.zeros(1, 2, 4, 2, dtype=torch.float64)
