@@ -6,10 +6,13 @@ package does not load the library; the first compute call does, and raises if
 the library has not been built (``build.build()``).
 """
 from . import balance, inputs  # noqa: F401
-from .binding import (RaError, all_to_all, block_units, check, forward, forward_block,  # noqa: F401
-                      forward_ulysses, lib, merge, permute, schedule_stats, schedule_units,
-                      set_kernel_variant, status_string, version, workspace_bytes)
+from .binding import (RaError, all_to_all, backward, backward_tile_pairs,  # noqa: F401
+                      backward_workspace_bytes, block_units, check, forward, forward_block, forward_ulysses, lib, merge,
+                      permute, schedule_stats, schedule_units, set_kernel_variant, status_string,
+                      version, workspace_bytes)
 
-__all__ = ["balance", "inputs", "RaError", "all_to_all", "block_units", "check", "forward",
+__all__ = ["balance", "inputs", "RaError", "all_to_all", "backward", "backward_tile_pairs",
+           "backward_workspace_bytes",
+           "block_units", "check", "forward",
            "forward_block", "forward_ulysses", "lib", "merge", "permute", "schedule_stats",
            "schedule_units", "set_kernel_variant", "status_string", "version", "workspace_bytes"]

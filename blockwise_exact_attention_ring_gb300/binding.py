@@ -57,6 +57,12 @@ def lib():
     L.ra_forward_rank_major.argtypes = [vp] * 5 + [i] * 10 + [vp, sz, vp]
     L.ra_forward_block.argtypes = [vp] * 5 + [i] * 11 + [vp]
     L.ra_all_to_all.argtypes = [vp, vp] + [i] * 7 + [vp]
+    L.ra_backward.argtypes = [vp] * 9 + [i] * 8 + [vp]
+    L.ra_backward_ws.argtypes = [vp] * 9 + [i] * 8 + [vp, sz, vp]
+    L.ra_backward_workspace_bytes.argtypes = [i] * 8
+    L.ra_backward_workspace_bytes.restype = sz
+    L.ra_backward_tile_pairs.argtypes = [i] * 8 + [vp, ll]
+    L.ra_backward_tile_pairs.restype = ll
     L.ra_ulysses_workspace_bytes.argtypes = [i] * 8
     L.ra_ulysses_workspace_bytes.restype = sz
     L.ra_forward_ulysses.argtypes = [vp] * 5 + [i] * 8 + [vp, sz, vp]
@@ -81,7 +87,7 @@ def lib():
     L.ra_schedule_stats.restype = ll
     for fn in ("ra_forward", "ra_forward_f32", "ra_forward_noalloc", "ra_forward_ws",
                "ra_forward_rank_major", "ra_forward_block", "ra_all_to_all", "ra_forward_ulysses",
-               "ra_permute", "ra_merge", "ra_check"):
+               "ra_backward", "ra_backward_ws", "ra_permute", "ra_merge", "ra_check"):
         getattr(L, fn).restype = i
     _lib = L
     return L
@@ -260,6 +266,49 @@ def forward_block(q, k, v, out_s, lse_s, n_blocks, rank, step, layout="contiguou
                                 LAYOUTS[layout], int(bool(causal)), DTYPES[q.dtype], int(rank),
                                 int(step), _stream(stream))
     _check(st, "ra_forward_block")
+
+
+def backward(q, k, v, out, lse, dout, n_blocks: int, layout: str = "contiguous", causal: bool = False,
+             workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of sum(dout * out) for (out, lse) = forward(q, k,
+    v, ...) with the same n_blocks, layout and causal (ra_backward / ra_backward_ws).
+    bf16 CUDA tensors in natural token order; lse fp32 [B,H,S]."""
+    B, H, Hkv, S, d = _dims(q, k, v)
+    if q.dtype != torch.bfloat16:
+        raise ValueError("the backward pass takes bf16 tensors")
+    for t, shape in ((out, q.shape), (dout, q.shape)):
+        if t.shape != shape or t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("out and dout must be contiguous bf16 CUDA tensors shaped like q")
+    if lse.shape != (B, H, S) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B,H,S] tensor")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    L = lib()
+    args = [_p(q), _p(k), _p(v), _p(out), _p(lse), _p(dout), _p(dq), _p(dk), _p(dv), B, H, Hkv, S, d,
+            n_blocks, LAYOUTS[layout], int(bool(causal))]
+    if workspace is None:
+        _check(L.ra_backward(*args, _stream(stream)), "ra_backward")
+    else:
+        _check(L.ra_backward_ws(*args, _p(workspace), workspace.numel() * workspace.element_size(),
+                                _stream(stream)), "ra_backward_ws")
+    return dq, dk, dv
+
+
+def backward_tile_pairs(B, H, Hkv, S, n_blocks, layout, causal, which):
+    """(query tile, key tile) pairs of the backward kernels in visiting order:
+    int array [n, 8] of (unit, bh, i, ta, j, tb, position, 0); which 0 = dK/dV
+    kernel, 1 = dQ kernel."""
+    L = lib()
+    args = (B, H, Hkv, S, n_blocks, LAYOUTS[layout], int(bool(causal)), int(which))
+    n = L.ra_backward_tile_pairs(*args, None, 0)
+    if n < 0:
+        raise ValueError("invalid schedule request")
+    out = np.zeros((n, 8), dtype=np.int32)
+    L.ra_backward_tile_pairs(*args, out.ctypes.data, n)
+    return out
+
+
+def backward_workspace_bytes(B, H, Hkv, S, d, n_blocks, layout="contiguous", causal=False) -> int:
+    return int(lib().ra_backward_workspace_bytes(B, H, Hkv, S, d, n_blocks, LAYOUTS[layout], int(causal)))
 
 
 def all_to_all(x: torch.Tensor, n_dev: int, inverse: bool = False,

@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/ra.h"
+#include "ra_bwd_schedule.h"
 #include "ra_internal.h"
 #include "ra_schedule.h"
 
@@ -211,24 +212,22 @@ struct RingCopies {
 
     bool make(cudaEvent_t &e) { return cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess; }
 
-    // copy t: every rank's block for step t into R[(t - 1) % 2]
+    // copy t: every rank's block for step t into R[(t - 1) % 2].  Rank i
+    // receives block (i - t) mod N from rank i - 1; over all ranks that is
+    // every block once, at the same offset in source and destination, so the
+    // N sends of a step are one copy of K and one of V (one call each keeps
+    // the host's enqueue cost off small steps).
     bool copy(int t)
     {
         const Problem &P = *p;
-        const size_t row = (size_t)P.d * P.esz(), blk = (size_t)P.L() * row, pitch = (size_t)P.S * row;
-        const size_t rows = (size_t)P.B * P.Hkv;
+        const size_t bytes = P.kv_elems() * P.esz();
         const char *sk = t == 1 ? k0 : rk[t % 2], *sv = t == 1 ? v0 : rv[t % 2];
         char *dk = rk[(t - 1) % 2], *dv = rv[(t - 1) % 2];
         if (t >= 3 && cudaStreamWaitEvent(cs, computed[t - 2], 0) != cudaSuccess)
             return false;
-        for (int i = 0; i < P.N; ++i) {
-            const size_t off = (size_t)ra_ring_block(i, t, P.N) * blk;  // block rank i receives
-            if (cudaMemcpy2DAsync(dk + off, pitch, sk + off, pitch, blk, rows, cudaMemcpyDeviceToDevice, cs) !=
-                    cudaSuccess ||
-                cudaMemcpy2DAsync(dv + off, pitch, sv + off, pitch, blk, rows, cudaMemcpyDeviceToDevice, cs) !=
-                    cudaSuccess)
-                return false;
-        }
+        if (cudaMemcpyAsync(dk, sk, bytes, cudaMemcpyDeviceToDevice, cs) != cudaSuccess ||
+            cudaMemcpyAsync(dv, sv, bytes, cudaMemcpyDeviceToDevice, cs) != cudaSuccess)
+            return false;
         return cudaEventRecord(copied[t], cs) == cudaSuccess;
     }
 
@@ -436,6 +435,95 @@ ra_status ulysses_plan(int B, int H, int Hkv, int S, int d, int n_dev, int causa
     return RA_OK;
 }
 
+// ------------------------------------------------------------------ backward
+// Workspace of the backward pass: delta (fp32 per row); for the striped
+// layout also rank-major copies of q, k, v, out, dout, lse and of the
+// gradients before they are put back in natural order.
+struct BwdWs {
+    size_t delta = 0, q = 0, k = 0, v = 0, out = 0, dout = 0, lse = 0, dq = 0, dk = 0, dv = 0, total = 0;
+};
+
+BwdWs bwd_ws_layout(const Problem &p)
+{
+    BwdWs w;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += align256(bytes);
+        return at;
+    };
+    w.delta = take(p.rows() * 4);
+    if (p.layout == RA_LAYOUT_STRIPED) {
+        const size_t qb = p.q_elems() * 2, kvb = p.kv_elems() * 2;
+        w.q = take(qb), w.k = take(kvb), w.v = take(kvb), w.out = take(qb), w.dout = take(qb);
+        w.lse = take(p.rows() * 4);
+        w.dq = take(qb), w.dk = take(kvb), w.dv = take(kvb);
+    }
+    w.total = off;
+    return w;
+}
+
+ra_status backward_impl(const Problem &p, const void *q, const void *k, const void *v, const void *out,
+                        const float *lse, const void *dout, void *dq, void *dk, void *dv, void *ws,
+                        size_t ws_bytes, cudaStream_t st)
+{
+    ra_status rs = check_problem(p);
+    if (rs != RA_OK)
+        return rs;
+    if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv)
+        return RA_ERR_INVALID_ARG;
+    const void *all[] = {q, k, v, out, lse, dout, dq, dk, dv};
+    for (const void *x : all)
+        if (!aligned16(x))
+            return RA_ERR_INVALID_ARG;
+    const size_t qb = p.q_elems() * 2, kvb = p.kv_elems() * 2, lb = p.rows() * 4;
+    const size_t sizes[] = {qb, kvb, kvb, qb, lb, qb, qb, kvb, kvb};
+    // the three gradients must not overlap any input or each other
+    for (int o = 6; o < 9; ++o)
+        for (int x = 0; x < 9; ++x)
+            if (x != o && overlaps(all[o], sizes[o], all[x], sizes[x]))
+                return RA_ERR_INVALID_ARG;
+    const BwdWs w = bwd_ws_layout(p);
+    if (!ws || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u))
+        return RA_ERR_WORKSPACE;
+    const int sm = sm_count_current();
+    char *base = static_cast<char *>(ws);
+    const bool striped = p.layout == RA_LAYOUT_STRIPED;
+    const long long row = (long long)p.d * 2;
+    const long long qrows = (long long)p.B * p.H * p.S, kvrows = (long long)p.B * p.Hkv * p.S;
+    ra::BwdLaunch a{};
+    a.q = q, a.k = k, a.v = v, a.out = out, a.dout = dout, a.lse = lse;
+    a.dq = dq, a.dk = dk, a.dv = dv;
+    if (striped) {
+        ra::launch_permute(q, base + w.q, qrows, p.S, p.N, row, 0, sm, st);
+        ra::launch_permute(k, base + w.k, kvrows, p.S, p.N, row, 0, sm, st);
+        ra::launch_permute(v, base + w.v, kvrows, p.S, p.N, row, 0, sm, st);
+        ra::launch_permute(out, base + w.out, qrows, p.S, p.N, row, 0, sm, st);
+        ra::launch_permute(dout, base + w.dout, qrows, p.S, p.N, row, 0, sm, st);
+        ra::launch_permute(lse, base + w.lse, qrows, p.S, p.N, 4, 0, sm, st);
+        count_launch(6);
+        if (cudaGetLastError() != cudaSuccess)
+            return RA_ERR_CUDA;
+        a.q = base + w.q, a.k = base + w.k, a.v = base + w.v, a.out = base + w.out, a.dout = base + w.dout;
+        a.lse = (const float *)(base + w.lse);
+        a.dq = base + w.dq, a.dk = base + w.dk, a.dv = base + w.dv;
+    }
+    a.delta = (float *)(base + w.delta);
+    a.B = p.B, a.H = p.H, a.Hkv = p.Hkv, a.S = p.S, a.d = p.d, a.N = p.N;
+    a.layout = p.layout, a.causal = p.causal;
+    a.timeout_ns = g_timeout_ns;
+    count_launch(3);
+    if (ra::launch_bwd(a, st) != cudaSuccess)
+        return RA_ERR_CUDA;
+    if (striped) {
+        ra::launch_permute(base + w.dq, dq, qrows, p.S, p.N, row, 1, sm, st);
+        ra::launch_permute(base + w.dk, dk, kvrows, p.S, p.N, row, 1, sm, st);
+        ra::launch_permute(base + w.dv, dv, kvrows, p.S, p.N, row, 1, sm, st);
+        count_launch(3);
+    }
+    return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -587,6 +675,79 @@ ra_status ra_forward_ulysses(const void *q, const void *k, const void *v, void *
     ra::launch_all_to_all(base + w.lse, lse, B, H, S, n_dev, 4, 1, sm, st);
     count_launch(2);
     return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+}
+
+long long ra_backward_tile_pairs(int B, int H, int Hkv, int S, int n_blocks, int layout, int causal, int which,
+                                 int *pairs, long long capacity)
+{
+    const Problem p{B, H, Hkv, S, 64, n_blocks, layout, causal, RA_DTYPE_BF16, RA_MODE_FUSED};
+    if (check_problem(p) != RA_OK || (which != 0 && which != 1))
+        return -1;
+    const int L = S / n_blocks, ntiles = (L + RA_TILE - 1) / RA_TILE, grp = H / Hkv;
+    const long long units = (long long)(which == 0 ? B * Hkv : B * H) * n_blocks * ntiles;
+    long long n = 0;
+    auto put = [&](long long u, int bh, int i, int ta, int j, int tb, long long k) {
+        if (pairs && n < capacity) {
+            int *o = pairs + 8 * n;
+            o[0] = (int)u, o[1] = bh, o[2] = i, o[3] = ta, o[4] = j, o[5] = tb, o[6] = (int)k, o[7] = 0;
+        }
+        ++n;
+    };
+    for (long long u = 0; u < units; ++u) {
+        long long k = 0;
+        if (which == 0) {
+            int bhkv, j, tb;
+            ra_bwd_dkdv_unit((int)u, B, Hkv, n_blocks, ntiles, layout, bhkv, j, tb);
+            const int b = bhkv / Hkv, g = bhkv % Hkv;
+            RaQWalk w;
+            for (w.start(j, tb, n_blocks, layout, causal, ntiles, grp); w.valid(); w.advance())
+                put(u, b * H + g * grp + w.hh, w.i, w.ta, j, tb, k++);
+        } else {
+            int bh, i, ta;
+            ra_bwd_dq_unit((int)u, B, H, n_blocks, ntiles, layout, bh, i, ta);
+            RaKWalk w;
+            for (w.start(i, ta, n_blocks, layout, causal, ntiles); w.valid(); w.advance())
+                put(u, bh, i, ta, w.j, w.tb, k++);
+        }
+    }
+    return n;
+}
+
+size_t ra_backward_workspace_bytes(int B, int H, int Hkv, int S, int d, int n_blocks, int layout, int causal)
+{
+    const Problem p{B, H, Hkv, S, d, n_blocks, layout, causal, RA_DTYPE_BF16, RA_MODE_FUSED};
+    if (check_problem(p) != RA_OK)
+        return 0;
+    return bwd_ws_layout(p).total;
+}
+
+ra_status ra_backward_ws(const void *q, const void *k, const void *v, const void *out, const float *lse,
+                         const void *dout, void *dq, void *dk, void *dv, int B, int H, int Hkv, int S, int d,
+                         int n_blocks, int layout, int causal, void *ws, size_t ws_bytes, ra_stream_t stream)
+{
+    const Problem p{B, H, Hkv, S, d, n_blocks, layout, causal, RA_DTYPE_BF16, RA_MODE_FUSED};
+    return backward_impl(p, q, k, v, out, lse, dout, dq, dk, dv, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+ra_status ra_backward(const void *q, const void *k, const void *v, const void *out, const float *lse,
+                      const void *dout, void *dq, void *dk, void *dv, int B, int H, int Hkv, int S, int d,
+                      int n_blocks, int layout, int causal, ra_stream_t stream)
+{
+    const Problem p{B, H, Hkv, S, d, n_blocks, layout, causal, RA_DTYPE_BF16, RA_MODE_FUSED};
+    ra_status rs = check_problem(p);
+    if (rs != RA_OK)
+        return rs;
+    cudaStream_t st = (cudaStream_t)stream;
+    const size_t bytes = bwd_ws_layout(p).total;
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, bytes, st) != cudaSuccess) {
+        cudaGetLastError();
+        return RA_ERR_NO_MEMORY;
+    }
+    rs = backward_impl(p, q, k, v, out, lse, dout, dq, dk, dv, ws, bytes, st);
+    if (cudaFreeAsync(ws, st) != cudaSuccess && rs == RA_OK)
+        rs = RA_ERR_CUDA;
+    return rs;
 }
 
 unsigned long long ra_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }

@@ -1,0 +1,676 @@
+// Backward pass of ring-ordered blockwise exact attention, sm_103a (GB300).
+//
+// The pages train through ring attention ("Context Parallelism" glossary
+// page, ultralytics.com/tr, section "Pratik Kullanim ve Odunlesimler": the
+// example calls backward on the attention output), and the ring computes
+// exact attention ("Ring Attention" page, section "Halka Dikkati Nasil
+// Calisir"), so the gradients are those of exact attention.  With the scale
+// c = 1/sqrt(d), the forward's log-sum-exp lse and delta = rowsum(dO * O):
+//
+//   P = exp(c Q K^T - lse)      dP = dO V^T      dS = P * (dP - delta)
+//   dV = P^T dO                 dK = c dS^T Q    dQ = c dS K
+//
+// computed blockwise in the ring's order.  On a ring, key/value block j and
+// its gradient accumulators travel: at step s they sit on device i = (j + s)
+// mod N, which adds the contribution of its query block i.  ra_bwd_dkdv_kernel
+// follows that order for one 128-key tile of block j (all query heads of the
+// kv group, query tiles that see the tile); ra_bwd_dq_kernel gives one
+// 128-row query tile its dQ over the key blocks j = (i - s) mod N, as the
+// forward walks them.  Both recompute P from lse instead of storing it.
+//
+// Per tile pair, on the tensor cores (tcgen05, fp32 accumulators in TMEM):
+//   dK/dV kernel: S^T = K Q^T and dP^T = V dO^T (SMEM x SMEM, keys on TMEM
+//     lanes); the elementwise warps turn them into P^T and dS^T (packed bf16,
+//     written back over the consumed columns); dV += P^T dO and
+//     dK += dS^T Q read them from TMEM as the A operand.
+//   dQ kernel: S = Q K^T and dP = dO V^T (queries on lanes); dS in TMEM;
+//     dQ += dS K.
+// Roles: warp 0 issues TMA loads (and stages lse / delta rows), warp 1 issues
+// MMAs and owns TMEM, warps 2-5 (one per TMEM lane quarter) do the
+// elementwise work and the epilogue.  Every wait is bounded, as in the
+// forward kernel.
+//
+// TMEM columns: S [0,128), dP [128,256), then the accumulators: dV and dK
+// (dK/dV kernel) or dQ (dQ kernel) from column 256.
+#include <cstdint>
+#include <cstring>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "ra_bwd_schedule.h"
+#include "ra_internal.h"
+#include "ra_ptx.cuh"
+
+namespace ra {
+
+namespace {
+
+constexpr int BWD_THREADS = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 elementwise
+constexpr uint32_t BWD_TMEM_COLS = 512;
+constexpr float LOG2E = 1.4426950408889634f;
+
+enum BwdSite : unsigned int {
+    BS_KV_FULL = 32, BS_ST_FULL, BS_ST_EMPTY, BS_S_FULL, BS_P_FULL, BS_FINAL, BS_Q_FULL, BS_KV_EMPTY,
+    BS_DRAIN
+};
+
+template <int D>
+struct BwdCfg {
+    static constexpr int SLAB = 128 * 64 * 2;
+    static constexpr int TILE = SLAB * (D / 64);
+    // dK/dV kernel: K, V once; Q and dO in two stages; lse/delta rows per stage
+    static constexpr int KV_OFF_K = 0;
+    static constexpr int KV_OFF_V = TILE;
+    static constexpr int KV_OFF_Q = 2 * TILE;
+    static constexpr int KV_OFF_DO = 4 * TILE;
+    static constexpr int KV_OFF_ROWS = 6 * TILE;           // [stage][nl | dl][128] floats
+    static constexpr int KV_OFF_CTRL = KV_OFF_ROWS + 2 * 2 * 128 * 4;
+    static constexpr int KV_SMEM = KV_OFF_CTRL + 256 + 1024;
+    // dQ kernel: Q, dO once; K and V in two stages
+    static constexpr int Q_OFF_Q = 0;
+    static constexpr int Q_OFF_DO = TILE;
+    static constexpr int Q_OFF_K = 2 * TILE;
+    static constexpr int Q_OFF_V = 4 * TILE;
+    static constexpr int Q_OFF_CTRL = 6 * TILE;
+    static constexpr int Q_SMEM = Q_OFF_CTRL + 256 + 1024;
+    // Both kernels allocate all 512 TMEM columns: ask for enough shared
+    // memory that a second CTA never lands on the same SM (it would block in
+    // tcgen05.alloc until the first one exits).
+    static constexpr int ONE_PER_SM = 120 * 1024;
+    static constexpr int KV_LAUNCH_SMEM = KV_SMEM > ONE_PER_SM ? KV_SMEM : ONE_PER_SM;
+    static constexpr int Q_LAUNCH_SMEM = Q_SMEM > ONE_PER_SM ? Q_SMEM : ONE_PER_SM;
+};
+
+struct BwdCtrl {
+    uint64_t once_full;            // K, V (dK/dV) or Q, dO (dQ)
+    uint64_t st_full[2], st_empty[2];
+    uint64_t s_full, p_full, final_bar;
+    uint32_t tmem_base;
+    int abort;
+};
+
+struct BwdParams {
+    CUtensorMap tm_q, tm_k, tm_v, tm_do;
+    const float *lse;    // [B H S] natural log, rank-major rows
+    const float *delta;  // [B H S]
+    __nv_bfloat16 *dq, *dk, *dv;
+    int B, H, Hkv, S, L, N, layout, causal, ntiles, n_units;
+    float scale, scale_log2;
+    unsigned long long timeout_ns;
+    unsigned int *status;  // the library's device status word
+};
+
+// Waits record a timeout in the library's status word (`st`, passed in by
+// the launch).
+__device__ __forceinline__ bool bwait(unsigned int *st, uint32_t bar, uint32_t parity, volatile int *abort,
+                                      uint64_t tmo, unsigned int site)
+{
+    return mbar_wait(bar, parity, abort, tmo, st, site);
+}
+
+__device__ __forceinline__ bool bwait_warp(unsigned int *st, uint32_t bar, uint32_t parity, volatile int *abort,
+                                           uint64_t tmo, unsigned int site)
+{
+    const bool ok = mbar_wait(bar, parity, abort, tmo, st, site);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void bdrain(unsigned int *st, uint32_t bar, uint32_t parity, uint64_t tmo)
+{
+    int never = 0;
+    mbar_wait(bar, parity, &never, tmo, st, BS_DRAIN);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                 "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+                 ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+                   "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
+                   "r"(r[13]), "r"(r[14]), "r"(r[15])
+                 : "memory");
+}
+
+template <int D>
+__device__ __forceinline__ void bload_tile(uint32_t dst, const CUtensorMap *tm, int row, uint32_t bar,
+                                           uint64_t pol)
+{
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h)
+        tma_load_2d(dst + h * BwdCfg<D>::SLAB, tm, h * 64, row, bar, pol);
+}
+
+// D (+)= A B^T over the head dimension: A, B are [128 rows][D] K-major tiles.
+template <int D>
+__device__ __forceinline__ void issue_rows_dot(uint32_t d_tmem, uint32_t a, uint32_t b)
+{
+    constexpr uint32_t ID = idesc_bf16_f32(128, 128, 0);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * BwdCfg<D>::SLAB + (kk & 3) * 32;
+        mma_ss(d_tmem, smem_desc_sw128(a + off, 16, 1024), smem_desc_sw128(b + off, 16, 1024), ID, kk > 0);
+    }
+}
+
+// D (+)= A[tmem, 128 x 128 bf16] B, B a [128 rows = K][D] tile read MN-major.
+template <int D>
+__device__ __forceinline__ void issue_tmem_times_tile(uint32_t d_tmem, uint32_t a_tmem, uint32_t b,
+                                                      bool accumulate)
+{
+    constexpr uint32_t ID = idesc_bf16_f32(128, D, 1);
+#pragma unroll
+    for (int kk = 0; kk < RA_TILE / 16; ++kk)
+        mma_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128(b + kk * 2048, BwdCfg<D>::SLAB, 1024), ID,
+               (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// ------------------------------------------------------------------ dK, dV
+template <int D>
+__global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dkdv_kernel(const __grid_constant__ BwdParams p)
+{
+    using C = BwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(smem);
+    BwdCtrl *ctrl = reinterpret_cast<BwdCtrl *>(smem + C::KV_OFF_CTRL);
+    float *rows = reinterpret_cast<float *>(smem + C::KV_OFF_ROWS);  // [st][nl|dl][128]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto bar = [&](uint64_t &b) { return smem_u32(&b); };
+
+    int bhkv, j, tb;
+    ra_bwd_dkdv_unit(blockIdx.x, p.B, p.Hkv, p.N, p.ntiles, p.layout, bhkv, j, tb);
+    const int b = bhkv / p.Hkv, g = bhkv % p.Hkv, grp = p.H / p.Hkv;
+    const int kvrow = bhkv * p.S + j * p.L + tb * RA_TILE;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(ctrl->once_full), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(ctrl->st_full[s]), 1);
+            mbar_init(bar(ctrl->st_empty[s]), 1);
+        }
+        mbar_init(bar(ctrl->s_full), 1);
+        mbar_init(bar(ctrl->p_full), 128);
+        mbar_init(bar(ctrl->final_bar), 1);
+        ctrl->abort = 0;
+        fence_mbar_init();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctrl->tmem_base), BWD_TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctrl->tmem_base;
+    volatile int *abort = &ctrl->abort;
+    const uint64_t tmo = p.timeout_ns;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        const uint64_t pol_kv = l2_policy_evict_first();
+        const uint64_t pol_q = l2_policy_evict_last();
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar(ctrl->once_full), 2 * C::TILE);
+            bload_tile<D>(sb + C::KV_OFF_K, &p.tm_k, kvrow, bar(ctrl->once_full), pol_kv);
+            bload_tile<D>(sb + C::KV_OFF_V, &p.tm_v, kvrow, bar(ctrl->once_full), pol_kv);
+        }
+        uint32_t n = 0;
+        bool ok = true;
+        RaQWalk w;
+        w.start(j, tb, p.N, p.layout, p.causal, p.ntiles, p.H / p.Hkv);
+        for (; w.valid(); w.advance(), ++n) {
+            const int st = n & 1;
+            if (n >= 2 && !(ok = bwait_warp(p.status, bar(ctrl->st_empty[st]), ((n >> 1) - 1) & 1, abort, tmo,
+                                            BS_ST_EMPTY)))
+                break;
+            const int bh = b * p.H + g * grp + w.hh;
+            const long long row0 = (long long)bh * p.S + (long long)w.i * p.L + w.ta * RA_TILE;
+            float *nl = rows + st * 256, *dl = nl + 128;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = lane + 32 * e;
+                const bool valid = w.ta * RA_TILE + r < p.L;
+                nl[r] = valid ? -p.lse[row0 + r] * LOG2E : 0.f;
+                dl[r] = valid ? p.delta[row0 + r] : 0.f;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar(ctrl->st_full[st]), 2 * C::TILE);
+                bload_tile<D>(sb + C::KV_OFF_Q + st * C::TILE, &p.tm_q, (int)row0, bar(ctrl->st_full[st]), pol_q);
+                bload_tile<D>(sb + C::KV_OFF_DO + st * C::TILE, &p.tm_do, (int)row0, bar(ctrl->st_full[st]),
+                              pol_q);
+            }
+            __syncwarp();
+        }
+        if (lane == 0) {
+            // every issued copy lands before shared memory is released
+            bdrain(p.status, bar(ctrl->once_full), 0, tmo);
+            for (uint32_t m = n > 2 ? n - 2 : 0; m < n; ++m)
+                bdrain(p.status, bar(ctrl->st_full[m & 1]), (m >> 1) & 1, tmo);
+        }
+        (void)ok;
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t sK = sb + C::KV_OFF_K, sV = sb + C::KV_OFF_V;
+            bool ok = bwait(p.status, bar(ctrl->once_full), 0, abort, tmo, BS_KV_FULL);
+            uint32_t n = 0;
+            RaQWalk w;
+            w.start(j, tb, p.N, p.layout, p.causal, p.ntiles, p.H / p.Hkv);
+            for (; ok && w.valid(); w.advance(), ++n) {
+                const int st = n & 1;
+                if (!(ok = bwait(p.status, bar(ctrl->st_full[st]), (n >> 1) & 1, abort, tmo, BS_ST_FULL)))
+                    break;
+                tc_fence_after();
+                const uint32_t sQ = sb + C::KV_OFF_Q + st * C::TILE, sDO = sb + C::KV_OFF_DO + st * C::TILE;
+                issue_rows_dot<D>(tmem, sK, sQ);          // S^T = K Q^T
+                issue_rows_dot<D>(tmem + 128, sV, sDO);   // dP^T = V dO^T
+                mma_commit(bar(ctrl->s_full));
+                if (!(ok = bwait(p.status, bar(ctrl->p_full), n & 1, abort, tmo, BS_P_FULL)))
+                    break;
+                tc_fence_after();
+                issue_tmem_times_tile<D>(tmem + 256, tmem, sDO, n > 0);        // dV += P^T dO
+                issue_tmem_times_tile<D>(tmem + 256 + D, tmem + 128, sQ, n > 0);  // dK += dS^T Q
+                mma_commit(bar(ctrl->st_empty[st]));
+            }
+            mma_commit(bar(ctrl->final_bar));
+            bdrain(p.status, bar(ctrl->final_bar), 0, tmo);
+        }
+    } else {
+        // ------------------------------------------------------------ elementwise
+        const int qw = warp & 3;
+        const int r = qw * 32 + lane;                 // key row of the tile
+        const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
+        const uint32_t tS = tmem + lane_off, tP = tS + 128;
+        const int bl = tb * RA_TILE + r;              // key local index in block j
+        const bool key_ok = bl < p.L;
+        const float sl2 = p.scale_log2;
+        uint32_t n = 0;
+        bool ok = true;
+        RaQWalk w;
+        w.start(j, tb, p.N, p.layout, p.causal, p.ntiles, p.H / p.Hkv);
+        for (; w.valid(); w.advance(), ++n) {
+            if (!(ok = bwait_warp(p.status, bar(ctrl->s_full), n & 1, abort, tmo, BS_S_FULL)))
+                break;
+            // the producer's lse / delta stores for this stage, made visible by
+            // the stage's own barrier (complete: S^T waited for it)
+            if (!(ok = bwait_warp(p.status, bar(ctrl->st_full[n & 1]), (n >> 1) & 1, abort, tmo, BS_ST_FULL)))
+                break;
+            tc_fence_after();
+            const float *nl = rows + (n & 1) * 256, *dl = nl + 128;
+            // visible iff lo <= a < hi for the query local index a
+            const int lo = !key_ok ? p.L : (w.cls == RA_CLS_FULL ? 0 : bl + (w.cls == RA_CLS_DIAG_EXCL ? 1 : 0));
+            const int hi = p.L;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t xs[32], xd[32];
+                tmem_ld32(tS + c * 32, xs);
+                tmem_ld32(tP + c * 32, xd);
+                tmem_wait_ld();
+                const int a0 = w.ta * RA_TILE + c * 32;
+                uint32_t pp[16], pd[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const int x = c * 32 + e;
+                    float p0 = ex2_approx(fmaf(__uint_as_float(xs[e]), sl2, nl[x]));
+                    float p1 = ex2_approx(fmaf(__uint_as_float(xs[e + 1]), sl2, nl[x + 1]));
+                    p0 = (a0 + e >= lo && a0 + e < hi) ? p0 : 0.f;
+                    p1 = (a0 + e + 1 >= lo && a0 + e + 1 < hi) ? p1 : 0.f;
+                    const float d0 = p0 * (__uint_as_float(xd[e]) - dl[x]);
+                    const float d1 = p1 * (__uint_as_float(xd[e + 1]) - dl[x + 1]);
+                    pp[e >> 1] = pack_bf16x2(p0, p1);
+                    pd[e >> 1] = pack_bf16x2(d0, d1);
+                }
+                // columns [16c, 16c + 16) were read in this or an earlier chunk
+                tmem_st16(tS + c * 16, pp);
+                tmem_st16(tP + c * 16, pd);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(ctrl->p_full));
+        }
+        // ------------------------------------------------------------ epilogue
+        if (ok)
+            ok = bwait_warp(p.status, bar(ctrl->final_bar), 0, abort, tmo, BS_FINAL);
+        if (ok) {
+            tc_fence_after();
+            const long long orow = (long long)kvrow + r;
+#pragma unroll 1
+            for (int which = 0; which < 2; ++which) {
+                __nv_bfloat16 *dst = which == 0 ? p.dv : p.dk;
+                const float mul = which == 0 ? 1.f : p.scale;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    __syncwarp();
+                    tmem_ld32(tS + 256 + which * D + c * 32, o);
+                    tmem_wait_ld();
+                    if (!key_ok)
+                        continue;
+                    uint4 *out = reinterpret_cast<uint4 *>(dst + orow * D + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        uint4 v;
+                        const bool z = (n == 0);  // no query tile met this key tile
+                        v.x = z ? 0u : pack_bf16x2(__uint_as_float(o[8 * e + 0]) * mul, __uint_as_float(o[8 * e + 1]) * mul);
+                        v.y = z ? 0u : pack_bf16x2(__uint_as_float(o[8 * e + 2]) * mul, __uint_as_float(o[8 * e + 3]) * mul);
+                        v.z = z ? 0u : pack_bf16x2(__uint_as_float(o[8 * e + 4]) * mul, __uint_as_float(o[8 * e + 5]) * mul);
+                        v.w = z ? 0u : pack_bf16x2(__uint_as_float(o[8 * e + 6]) * mul, __uint_as_float(o[8 * e + 7]) * mul);
+                        out[e] = v;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, BWD_TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ dQ
+template <int D>
+__global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dq_kernel(const __grid_constant__ BwdParams p)
+{
+    using C = BwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(smem);
+    BwdCtrl *ctrl = reinterpret_cast<BwdCtrl *>(smem + C::Q_OFF_CTRL);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto bar = [&](uint64_t &b) { return smem_u32(&b); };
+
+    int bh, i, ta;
+    ra_bwd_dq_unit(blockIdx.x, p.B, p.H, p.N, p.ntiles, p.layout, bh, i, ta);
+    const int b = bh / p.H, h = bh % p.H;
+    const int kvbh = b * p.Hkv + h / (p.H / p.Hkv);
+    const int qrow = bh * p.S + i * p.L + ta * RA_TILE;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(ctrl->once_full), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(ctrl->st_full[s]), 1);
+            mbar_init(bar(ctrl->st_empty[s]), 1);
+        }
+        mbar_init(bar(ctrl->s_full), 1);
+        mbar_init(bar(ctrl->p_full), 128);
+        mbar_init(bar(ctrl->final_bar), 1);
+        ctrl->abort = 0;
+        fence_mbar_init();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctrl->tmem_base), BWD_TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctrl->tmem_base;
+    volatile int *abort = &ctrl->abort;
+    const uint64_t tmo = p.timeout_ns;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol_q = l2_policy_evict_first();
+            const uint64_t pol_kv = l2_policy_evict_last();
+            mbar_arrive_expect_tx(bar(ctrl->once_full), 2 * C::TILE);
+            bload_tile<D>(sb + C::Q_OFF_Q, &p.tm_q, qrow, bar(ctrl->once_full), pol_q);
+            bload_tile<D>(sb + C::Q_OFF_DO, &p.tm_do, qrow, bar(ctrl->once_full), pol_q);
+            uint32_t n = 0;
+            bool ok = true;
+            RaKWalk w;
+            w.start(i, ta, p.N, p.layout, p.causal, p.ntiles);
+            for (; w.valid(); w.advance(), ++n) {
+                const int st = n & 1;
+                if (n >= 2 && !(ok = bwait(p.status, bar(ctrl->st_empty[st]), ((n >> 1) - 1) & 1, abort, tmo, BS_KV_EMPTY)))
+                    break;
+                const int row = kvbh * p.S + w.j * p.L + w.tb * RA_TILE;
+                mbar_arrive_expect_tx(bar(ctrl->st_full[st]), 2 * C::TILE);
+                bload_tile<D>(sb + C::Q_OFF_K + st * C::TILE, &p.tm_k, row, bar(ctrl->st_full[st]), pol_kv);
+                bload_tile<D>(sb + C::Q_OFF_V + st * C::TILE, &p.tm_v, row, bar(ctrl->st_full[st]), pol_kv);
+            }
+            bdrain(p.status, bar(ctrl->once_full), 0, tmo);
+            for (uint32_t m = n > 2 ? n - 2 : 0; m < n; ++m)
+                bdrain(p.status, bar(ctrl->st_full[m & 1]), (m >> 1) & 1, tmo);
+            (void)ok;
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t sQ = sb + C::Q_OFF_Q, sDO = sb + C::Q_OFF_DO;
+            bool ok = bwait(p.status, bar(ctrl->once_full), 0, abort, tmo, BS_Q_FULL);
+            uint32_t n = 0;
+            RaKWalk w;
+            w.start(i, ta, p.N, p.layout, p.causal, p.ntiles);
+            for (; ok && w.valid(); w.advance(), ++n) {
+                const int st = n & 1;
+                if (!(ok = bwait(p.status, bar(ctrl->st_full[st]), (n >> 1) & 1, abort, tmo, BS_ST_FULL)))
+                    break;
+                tc_fence_after();
+                const uint32_t sK = sb + C::Q_OFF_K + st * C::TILE, sV = sb + C::Q_OFF_V + st * C::TILE;
+                issue_rows_dot<D>(tmem, sQ, sK);          // S = Q K^T
+                issue_rows_dot<D>(tmem + 128, sDO, sV);   // dP = dO V^T
+                mma_commit(bar(ctrl->s_full));
+                if (!(ok = bwait(p.status, bar(ctrl->p_full), n & 1, abort, tmo, BS_P_FULL)))
+                    break;
+                tc_fence_after();
+                issue_tmem_times_tile<D>(tmem + 256, tmem, sK, n > 0);  // dQ += dS K
+                mma_commit(bar(ctrl->st_empty[st]));
+            }
+            mma_commit(bar(ctrl->final_bar));
+            bdrain(p.status, bar(ctrl->final_bar), 0, tmo);
+        }
+    } else {
+        const int qw = warp & 3;
+        const int r = qw * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
+        const uint32_t tS = tmem + lane_off, tP = tS + 128;
+        const int a = ta * RA_TILE + r;
+        const bool row_ok = a < p.L;
+        const long long grow = (long long)qrow + r;
+        const float nl = row_ok ? -p.lse[grow] * LOG2E : 0.f;
+        const float dl = row_ok ? p.delta[grow] : 0.f;
+        const float sl2 = p.scale_log2;
+        uint32_t n = 0;
+        bool ok = true;
+        RaKWalk w;
+        w.start(i, ta, p.N, p.layout, p.causal, p.ntiles);
+        for (; w.valid(); w.advance(), ++n) {
+            if (!(ok = bwait_warp(p.status, bar(ctrl->s_full), n & 1, abort, tmo, BS_S_FULL)))
+                break;
+            tc_fence_after();
+            const int lim = row_ok ? ra_key_limit(w.cls, a, p.L) - w.tb * RA_TILE : 0;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t xs[32], xd[32];
+                tmem_ld32(tS + c * 32, xs);
+                tmem_ld32(tP + c * 32, xd);
+                tmem_wait_ld();
+                uint32_t pd[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const int x = c * 32 + e;
+                    float p0 = ex2_approx(fmaf(__uint_as_float(xs[e]), sl2, nl));
+                    float p1 = ex2_approx(fmaf(__uint_as_float(xs[e + 1]), sl2, nl));
+                    p0 = x < lim ? p0 : 0.f;
+                    p1 = x + 1 < lim ? p1 : 0.f;
+                    pd[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(xd[e]) - dl),
+                                             p1 * (__uint_as_float(xd[e + 1]) - dl));
+                }
+                tmem_st16(tS + c * 16, pd);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(ctrl->p_full));
+        }
+        if (ok)
+            ok = bwait_warp(p.status, bar(ctrl->final_bar), 0, abort, tmo, BS_FINAL);
+        if (ok) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                __syncwarp();
+                tmem_ld32(tS + 256 + c * 32, o);
+                tmem_wait_ld();
+                if (!row_ok)
+                    continue;
+                uint4 *out = reinterpret_cast<uint4 *>(p.dq + grow * D + c * 32);
+                const float mul = p.scale;
+                const bool z = (n == 0);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    uint4 v;
+                    v.x = z ? 0u : pack_bf16x2(__uint_as_float(o[8 * e + 0]) * mul, __uint_as_float(o[8 * e + 1]) * mul);
+                    v.y = z ? 0u : pack_bf16x2(__uint_as_float(o[8 * e + 2]) * mul, __uint_as_float(o[8 * e + 3]) * mul);
+                    v.z = z ? 0u : pack_bf16x2(__uint_as_float(o[8 * e + 4]) * mul, __uint_as_float(o[8 * e + 5]) * mul);
+                    v.w = z ? 0u : pack_bf16x2(__uint_as_float(o[8 * e + 6]) * mul, __uint_as_float(o[8 * e + 7]) * mul);
+                    out[e] = v;
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, BWD_TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ delta
+// delta[row] = sum_c dO[row, c] O[row, c] in fp32; each thread takes 8
+// columns (16 bytes), D / 8 threads per row reduce with shuffles.
+template <int D>
+__global__ void ra_bwd_delta_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dout,
+                                    float *__restrict__ delta, long long rows)
+{
+    constexpr int G = D / 8;  // threads per row
+    const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long row = t / G;
+    const int part = (int)(t % G);
+    float acc = 0.f;
+    if (row < rows) {
+        const uint4 x = reinterpret_cast<const uint4 *>(o + row * D)[part];
+        const uint4 y = reinterpret_cast<const uint4 *>(dout + row * D)[part];
+        const __nv_bfloat162 *xa = reinterpret_cast<const __nv_bfloat162 *>(&x);
+        const __nv_bfloat162 *ya = reinterpret_cast<const __nv_bfloat162 *>(&y);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 fx = __bfloat1622float2(xa[e]), fy = __bfloat1622float2(ya[e]);
+            acc = fmaf(fx.x, fy.x, acc);
+            acc = fmaf(fx.y, fy.y, acc);
+        }
+    }
+#pragma unroll
+    for (int off = G / 2; off > 0; off >>= 1)
+        acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (row < rows && part == 0)
+        delta[row] = acc;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 bwd_encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void *ptr = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+bool bwd_encode_rows(CUtensorMap *tm, const void *base, long long rows, int d)
+{
+    auto enc = bwd_encode_fn();
+    if (!enc)
+        return false;
+    cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+    cuuint32_t box[2] = {64, RA_TILE};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdLaunch &a, cudaStream_t st)
+{
+    using C = BwdCfg<D>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(ra_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::KV_LAUNCH_SMEM);
+        if (e != cudaSuccess)
+            return e;
+        e = cudaFuncSetAttribute(ra_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::Q_LAUNCH_SMEM);
+        if (e != cudaSuccess)
+            return e;
+        attr_set = true;
+    }
+    const long long rows = (long long)a.B * a.H * a.S;
+    {
+        const long long threads = rows * (D / 8);
+        const int block = 256;
+        ra_bwd_delta_kernel<D><<<(unsigned)((threads + block - 1) / block), block, 0, st>>>(
+            static_cast<const __nv_bfloat16 *>(a.out), static_cast<const __nv_bfloat16 *>(a.dout), a.delta, rows);
+    }
+    BwdParams p;
+    memset(&p, 0, sizeof(p));
+    if (!bwd_encode_rows(&p.tm_q, a.q, rows, D) ||
+        !bwd_encode_rows(&p.tm_k, a.k, (long long)a.B * a.Hkv * a.S, D) ||
+        !bwd_encode_rows(&p.tm_v, a.v, (long long)a.B * a.Hkv * a.S, D) ||
+        !bwd_encode_rows(&p.tm_do, a.dout, rows, D))
+        return cudaErrorInvalidValue;
+    p.lse = a.lse, p.delta = a.delta;
+    p.dq = static_cast<__nv_bfloat16 *>(a.dq);
+    p.dk = static_cast<__nv_bfloat16 *>(a.dk);
+    p.dv = static_cast<__nv_bfloat16 *>(a.dv);
+    p.B = a.B, p.H = a.H, p.Hkv = a.Hkv, p.S = a.S, p.N = a.N, p.L = a.S / a.N;
+    p.layout = a.layout, p.causal = a.causal;
+    p.ntiles = (p.L + RA_TILE - 1) / RA_TILE;
+    p.scale = 1.0f / sqrtf((float)D);
+    p.scale_log2 = LOG2E / sqrtf((float)D);
+    p.timeout_ns = a.timeout_ns;
+    p.status = device_status_ptr();
+    if (!p.status)
+        return cudaErrorInvalidValue;
+    const long long kv_units = (long long)a.B * a.Hkv * a.N * p.ntiles;
+    const long long q_units = (long long)a.B * a.H * a.N * p.ntiles;
+    if (kv_units > 0x7fffffffll || q_units > 0x7fffffffll)
+        return cudaErrorInvalidValue;
+    p.n_units = (int)kv_units;
+    ra_bwd_dkdv_kernel<D><<<(unsigned)kv_units, BWD_THREADS, C::KV_LAUNCH_SMEM, st>>>(p);
+    p.n_units = (int)q_units;
+    ra_bwd_dq_kernel<D><<<(unsigned)q_units, BWD_THREADS, C::Q_LAUNCH_SMEM, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdLaunch &a, cudaStream_t st)
+{
+    if (a.d == 128)
+        return launch_bwd_d<128>(a, st);
+    if (a.d == 64)
+        return launch_bwd_d<64>(a, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace ra

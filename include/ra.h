@@ -80,7 +80,9 @@ typedef enum { RA_LAYOUT_CONTIGUOUS = 0, RA_LAYOUT_STRIPED = 1 } ra_layout;
  * RA_MODE_RING: RA_MODE_PER_STEP with the key/value rotation made explicit:
  *   before step s every rank's block is copied (by the copy engine, on a
  *   second stream of the library's own) from where the previous rank held it
- *   into a double-buffered workspace copy, and step s reads that copy.  The
+ *   into a double-buffered workspace copy, and step s reads that copy (the
+ *   N sends of a step land at the blocks' own offsets, so they are issued as
+ *   one copy of k and one of v).  The
  *   copy for step s + 1 overlaps the compute of step s, as the send of the
  *   block to the next device overlaps the block computation on a real ring
  *   ("Ring Attention" page, section "Halka Dikkati Nasil Calisir": each device
@@ -234,6 +236,45 @@ ra_status ra_forward_ulysses(const void *q, const void *k, const void *v, void *
                              ra_stream_t stream);
 
 /*
+ * ra_backward - gradients of ring attention: dq, dk, dv of the loss
+ * sum(dout * out) where (out, lse) = ra_forward(q, k, v, ...).  The pages
+ * train through the ring ("Context Parallelism" glossary page, section
+ * "Pratik Kullanim ve Odunlesimler": the example calls backward on the
+ * attention output); the ring is exact, so these are the gradients of exact
+ * attention, computed blockwise in ring order from the saved lse:
+ *   P = exp(q k^T / sqrt(d) - lse), dS = P * (dout v^T - rowsum(dout * out)),
+ *   dv = P^T dout, dk = dS^T q / sqrt(d), dq = dS k / sqrt(d)
+ * (GQA: dk, dv summed over each kv head's query heads).  Key/value block j's
+ * gradients accumulate over query blocks i = (j + s) mod N, s = 0..N-1, the
+ * order in which they would travel around the ring.
+ *   q, out, dout, dq: bf16 [B,H,S,d]; k, v, dk, dv: bf16 [B,Hkv,S,d];
+ *   lse: fp32 [B,H,S] as ra_forward wrote it; natural token order; layout,
+ *   causal and n_blocks as given to ra_forward.
+ * d in {64, 128} (RA_ERR_UNSUPPORTED otherwise); any L >= 1.  Device
+ * pointers, 16-byte aligned, caller-owned; dq, dk, dv must not overlap any
+ * other argument (RA_ERR_INVALID_ARG).  Scratch is allocated stream-ordered
+ * (RA_ERR_NO_MEMORY); asynchronous on `stream`; a device-side timeout is
+ * reported by ra_check.
+ */
+ra_status ra_backward(const void *q, const void *k, const void *v, const void *out,
+                      const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                      int B, int H, int Hkv, int S, int d, int n_blocks, int layout,
+                      int causal, ra_stream_t stream);
+
+/* ra_backward_workspace_bytes - scratch ra_backward_ws needs (delta per row;
+ * for the striped layout, rank-major copies of the inputs and gradients);
+ * 0 for an invalid request. */
+size_t ra_backward_workspace_bytes(int B, int H, int Hkv, int S, int d, int n_blocks,
+                                   int layout, int causal);
+
+/* ra_backward_ws - ra_backward with a caller-owned workspace (256-byte
+ * aligned, at least ra_backward_workspace_bytes; RA_ERR_WORKSPACE). */
+ra_status ra_backward_ws(const void *q, const void *k, const void *v, const void *out,
+                         const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                         int B, int H, int Hkv, int S, int d, int n_blocks, int layout,
+                         int causal, void *ws, size_t ws_bytes, ra_stream_t stream);
+
+/*
  * ra_forward_noalloc - ra_forward for callers that cannot allocate device
  * memory.  No counterpart on the pages: this is a deployment variant of the
  * same computation, with the same arguments, result and error rules as
@@ -380,6 +421,20 @@ long long ra_schedule_units(int B, int H, int Hkv, int S, int n_blocks, int layo
  */
 long long ra_schedule_block_units(int B, int H, int Hkv, int S, int n_blocks, int layout, int causal,
                                   int rank, int step, int *units, long long capacity);
+
+/*
+ * ra_backward_tile_pairs - host-only view of the backward pass's work: the
+ * (query tile, key tile) pairs each kernel visits, unit by unit, in order.
+ * which = 0: the dK/dV kernel (one unit per 128-key tile; query blocks in the
+ * order the key block travels the ring, i = (j + s) mod N); which = 1: the dQ
+ * kernel (one unit per 128-row query tile; key blocks j = (i - s) mod N).
+ * Pair n is written to pairs[8n .. 8n + 7] as {unit, batch*H + query head,
+ * query block i, query tile ta, key block j, key tile tb, position within the
+ * unit, 0}.  Writes at most `capacity` pairs (pairs may be NULL); returns the
+ * total, or -1 on bad input.  Source: as for ra_backward.
+ */
+long long ra_backward_tile_pairs(int B, int H, int Hkv, int S, int n_blocks, int layout,
+                                 int causal, int which, int *pairs, long long capacity);
 
 #ifdef __cplusplus
 }

@@ -83,3 +83,50 @@ def test_measured_summary_matches_model_on_model_input():
         "critical_path"]
     with pytest.raises(ValueError):
         balance.summarize(np.zeros((2, 3)))
+
+
+def _visible_tile_pairs(B, H, S, N, layout, causal):
+    """(bh, i, ta, j, tb) for every query tile / key tile pair with a visible
+    (query, key) pair, from the causal rule on natural positions."""
+    import oracle
+    L = S // N
+    nt = -(-L // 128)
+    order = oracle.stripe_order(S, N) if layout == "striped" else np.arange(S)
+    pos = order.reshape(N, L)
+    out = set()
+    for i in range(N):
+        for ta in range(nt):
+            t = pos[i][ta * 128:(ta + 1) * 128]
+            for j in range(N):
+                for tb in range(nt):
+                    u = pos[j][tb * 128:(tb + 1) * 128]
+                    if not causal or (u[None, :] <= t[:, None]).any():
+                        for bh in range(B * H):
+                            out.add((bh, i, ta, j, tb))
+    return out
+
+
+@pytest.mark.parametrize("B,H,Hkv,S,N", [(1, 4, 2, 1024, 4), (2, 3, 1, 768, 3), (1, 2, 2, 640, 5)])
+@pytest.mark.parametrize("layout,causal", [("contiguous", True), ("striped", True), ("contiguous", False)])
+def test_backward_kernels_cover_every_visible_tile_pair_once(B, H, Hkv, S, N, layout, causal):
+    """Both backward kernels visit exactly the tile pairs with a visible key,
+    each once; the dK/dV kernel meets query blocks in the order the key block
+    travels (i = j, j + 1, ...) and the dQ kernel key blocks in the forward's
+    order (j = i, i - 1, ...)."""
+    want = _visible_tile_pairs(B, H, S, N, layout, causal)
+    for which in (0, 1):
+        pairs = ra.backward_tile_pairs(B, H, Hkv, S, N, layout, causal, which)
+        got = [tuple(r) for r in pairs[:, 1:6].tolist()]
+        assert len(got) == len(set(got)) == len(want), which
+        assert set(got) == want, which
+        for u in np.unique(pairs[:, 0]):
+            rows = pairs[pairs[:, 0] == u]
+            assert np.array_equal(rows[:, 6], np.arange(len(rows)))
+            steps = (rows[:, 2] - rows[:, 4]) % N if which == 0 else (rows[:, 2] - rows[:, 4]) % N
+            assert np.all(np.diff(steps) >= 0), (which, u)
+            if which == 0:
+                grp = H // Hkv
+                assert len(set((rows[:, 1] // H * Hkv + rows[:, 1] % H // grp).tolist())) == 1
+                assert len(set(rows[:, 4].tolist())) == 1 and len(set(rows[:, 5].tolist())) == 1
+            else:
+                assert len(set(rows[:, 1].tolist())) == 1 and len(set(rows[:, 3].tolist())) == 1

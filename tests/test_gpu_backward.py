@@ -1,0 +1,130 @@
+"""Backward pass (ra_backward) against the fp64 oracle of the gradients of
+exact attention.
+
+Tolerance: every gradient is a sum of products in which one factor (P, dS,
+and out through delta) is rounded to bf16 (relative 2^-9) before an fp32
+accumulation, and the result is rounded to bf16 again; with cancellation in
+dS = P (dP - delta) the error is bounded relative to the tensor's largest
+entry, not entrywise.  The bar is max |got - ref| <= 2e-2 max |ref| per
+tensor (the bf16 output bar of the forward, scaled to the gradient's size),
+and the mean error <= 2e-3 max |ref|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import blockwise_exact_attention_ring_gb300 as ra
+from blockwise_exact_attention_ring_gb300 import inputs
+from oracle.backward import attention_backward, dq_rows
+
+pytestmark = pytest.mark.gpu
+
+REL_MAX, REL_MEAN = 2e-2, 2e-3
+
+
+def _dout(B, H, S, d, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(B, H, S, d, generator=g).to(torch.bfloat16)
+
+
+def _check(got, ref, what):
+    got = got.float().cpu().double().numpy()
+    scale = np.abs(ref).max()
+    err = np.abs(got - ref)
+    assert err.max() <= REL_MAX * scale, f"{what}: max err {err.max():.3g} vs scale {scale:.3g}"
+    assert err.mean() <= REL_MEAN * scale, f"{what}: mean err {err.mean():.3g} vs scale {scale:.3g}"
+
+
+CASES = [
+    # B, H, Hkv, S, d, N, layout, causal
+    (1, 2, 1, 256, 64, 2, "contiguous", True),
+    (1, 4, 2, 1024, 128, 4, "striped", True),
+    (1, 4, 2, 1024, 128, 4, "contiguous", True),
+    (2, 2, 2, 512, 64, 1, "contiguous", False),
+    (1, 2, 1, 600, 128, 3, "striped", True),      # L = 200: ragged tiles
+    (1, 4, 4, 384, 128, 3, "contiguous", False),
+    (1, 6, 2, 768, 64, 2, "striped", False),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "B{}H{}kv{}S{}d{}N{}-{}-{}".format(*c))
+def test_backward_matches_oracle(case):
+    B, H, Hkv, S, d, N, layout, causal = case
+    q, k, v = inputs.make_qkv(B, H, Hkv, S, d, seed=S + 3 * d + N)
+    dout = _dout(B, H, S, d, seed=S + 1)
+    qd, kd, vd, dod = (t.cuda().contiguous() for t in (q, k, v, dout))
+    out, lse = ra.forward(qd, kd, vd, n_blocks=N, layout=layout, causal=causal)
+    dq, dk, dv = ra.backward(qd, kd, vd, out, lse, dod, N, layout=layout, causal=causal)
+    ra.check()
+    rq, rk, rv = attention_backward(q, k, v, dout, causal)
+    _check(dq, rq, "dq")
+    _check(dk, rk, "dk")
+    _check(dv, rv, "dv")
+
+
+def test_backward_independent_of_ring_size_and_layout():
+    """Same tokens, any N and layout: the same gradients up to rounding."""
+    B, H, Hkv, S, d = 1, 4, 2, 1536, 128
+    q, k, v = (t.cuda() for t in inputs.make_qkv(B, H, Hkv, S, d, seed=8))
+    dout = _dout(B, H, S, d, seed=9).cuda()
+    base = None
+    for N, layout in [(1, "contiguous"), (3, "contiguous"), (4, "striped"), (6, "striped")]:
+        out, lse = ra.forward(q, k, v, n_blocks=N, layout=layout, causal=True)
+        g = ra.backward(q, k, v, out, lse, dout, N, layout=layout, causal=True)
+        ra.check()
+        if base is None:
+            base = g
+            continue
+        for a, b in zip(base, g):
+            scale = a.float().abs().max().item()
+            assert (a.float() - b.float()).abs().max().item() <= 2e-2 * scale
+
+
+def test_backward_deterministic():
+    q, k, v = (t.cuda() for t in inputs.make_qkv(1, 4, 2, 1024, 128, seed=4))
+    dout = _dout(1, 4, 1024, 128, seed=5).cuda()
+    out, lse = ra.forward(q, k, v, n_blocks=4, layout="striped", causal=True)
+    a = ra.backward(q, k, v, out, lse, dout, 4, layout="striped", causal=True)
+    b = ra.backward(q, k, v, out, lse, dout, 4, layout="striped", causal=True)
+    ra.check()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_backward_workload_32k_properties_and_sampled_rows():
+    """32K tokens, 32 query heads over 8 kv heads, causal, N = 4 (the 32K
+    workload's shape): dq on sampled rows against the oracle row by row, and
+    over all keys the identities sum_u dV = sum_t dO (per kv head) and
+    sum_u dK = 0, which the whole dK and dV must satisfy."""
+    w = inputs.WORKLOADS["ring4-s32k-h32kv8-d128-causal-contiguous"]
+    q, k, v = inputs.workload_qkv(w, device="cuda")
+    dout = _dout(w.B, w.H, w.S, w.d, seed=77).cuda()
+    out, lse = ra.forward(q, k, v, n_blocks=w.n_blocks, layout="striped", causal=True)
+    dq, dk, dv = ra.backward(q, k, v, out, lse, dout, w.n_blocks, layout="striped", causal=True)
+    ra.check()
+    rows = inputs.sample_rows(w.B, w.H, w.S, w.n_blocks, n=96, seed=7)
+    ref = dq_rows(q.cpu(), k.cpu(), v.cpu(), dout.cpu(), rows, causal=True)
+    got = dq.float().cpu().double().numpy().reshape(-1, w.d)[rows]
+    assert np.abs(got - ref).max() <= REL_MAX * np.abs(ref).max()
+    grp = w.H // w.Hkv
+    dv_sum = dv.double().sum(dim=2)
+    do_sum = dout.double().reshape(w.B, w.Hkv, grp, w.S, w.d).sum(dim=(2, 3))
+    assert (dv_sum - do_sum).abs().max().item() <= 1e-2 * dout.double().abs().sum(dim=2).max().item()
+    dk_sum = dk.double().sum(dim=2)
+    assert dk_sum.abs().max().item() <= 1e-2 * dk.double().abs().sum(dim=2).max().item()
+
+
+def test_backward_rejects_bad_arguments():
+    q, k, v = (t.cuda() for t in inputs.make_qkv(1, 2, 1, 256, 64, seed=1))
+    out, lse = ra.forward(q, k, v, n_blocks=2, causal=True)
+    dout = torch.zeros_like(q)
+    L = ra.lib()
+    P = lambda t: t.data_ptr()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    # dq aliasing q
+    assert L.ra_backward(P(q), P(k), P(v), P(out), P(lse), P(dout), P(q), P(dk), P(dv),
+                         1, 2, 1, 256, 64, 2, 0, 1, None) == 1
+    # d = 32 is not a tensor-core head dimension
+    assert L.ra_backward(P(q), P(k), P(v), P(out), P(lse), P(dout), P(dq), P(dk), P(dv),
+                         1, 2, 1, 512, 32, 2, 0, 1, None) == 2
+    ra.check()
