@@ -26,8 +26,8 @@
 //   dQ kernel: S = Q K^T and dP = dO V^T (queries on lanes); dS in TMEM;
 //     dQ += dS K.
 // Roles: warp 0 issues TMA loads (and stages lse / delta rows), warp 1 issues
-// MMAs and owns TMEM, warps 2-5 (one per TMEM lane quarter) do the
-// elementwise work and the epilogue.  Every wait is bounded, as in the
+// MMAs and owns TMEM, warps 2-9 (two per TMEM lane quarter, each on half of
+// the columns) do the elementwise work and the epilogue.  Every wait is bounded, as in the
 // forward kernel.
 //
 // TMEM columns: S [0,128), dP [128,256), then the accumulators: dV and dK
@@ -47,7 +47,8 @@ namespace ra {
 
 namespace {
 
-constexpr int BWD_THREADS = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 elementwise
+constexpr int BWD_THREADS = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 elementwise (2 per lane quarter)
+constexpr int BWD_EW = 256;       // elementwise threads
 constexpr uint32_t BWD_TMEM_COLS = 512;
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -86,7 +87,12 @@ struct BwdCfg {
 struct BwdCtrl {
     uint64_t once_full;            // K, V (dK/dV) or Q, dO (dQ)
     uint64_t st_full[2], st_empty[2];
-    uint64_t s_full, p_full, final_bar;
+    uint64_t s_full[2];            // S (per S buffer)
+    uint64_t dp_full;              // dP
+    uint64_t p_full;               // dK/dV: P^T written; dQ: dS written (256 arrivals)
+    uint64_t ds_full;              // dK/dV: dS^T written (256 arrivals)
+    uint64_t pair[4];              // the two warps of a TMEM lane quarter (64 arrivals)
+    uint64_t final_bar;
     uint32_t tmem_base;
     int abort;
 };
@@ -166,7 +172,64 @@ __device__ __forceinline__ void issue_tmem_times_tile(uint32_t d_tmem, uint32_t 
                (accumulate || kk > 0) ? 1u : 0u);
 }
 
+// Iterations of one unit (tile pairs it visits), counted per ring step.
+__device__ __forceinline__ int dkdv_count(int j, int tb, const BwdParams &p)
+{
+    int n = 0;
+    for (int s = 0; s < p.N; ++s) {
+        const int cls = ra_block_class(p.layout, p.causal, (j + s) % p.N, j);
+        const int first = cls == RA_CLS_FULL ? 0 : tb;
+        if (cls != RA_CLS_SKIP && first < p.ntiles)
+            n += (p.H / p.Hkv) * (p.ntiles - first);
+    }
+    return n;
+}
+
+__device__ __forceinline__ int dq_count(int i, int ta, const BwdParams &p)
+{
+    int n = 0;
+    for (int s = 0; s < p.N; ++s)
+        n += ra_kv_tiles(ra_block_class(p.layout, p.causal, i, ra_ring_block(i, s, p.N)), ta, p.ntiles);
+    return n;
+}
+
+__device__ __forceinline__ void bwd_init_barriers(BwdCtrl *ctrl)
+{
+    mbar_init(smem_u32(&ctrl->once_full), 1);
+    for (int s = 0; s < 2; ++s) {
+        mbar_init(smem_u32(&ctrl->st_full[s]), 1);
+        mbar_init(smem_u32(&ctrl->st_empty[s]), 1);
+        mbar_init(smem_u32(&ctrl->s_full[s]), 1);
+    }
+    mbar_init(smem_u32(&ctrl->dp_full), 1);
+    mbar_init(smem_u32(&ctrl->p_full), BWD_EW);
+    mbar_init(smem_u32(&ctrl->ds_full), BWD_EW);
+    for (int q = 0; q < 4; ++q)
+        mbar_init(smem_u32(&ctrl->pair[q]), 64);
+    mbar_init(smem_u32(&ctrl->final_bar), 1);
+    ctrl->abort = 0;
+    fence_mbar_init();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 pack8(const uint32_t (&o)[32], int e, float mul, bool zero)
+{
+    uint4 v;
+    v.x = zero ? 0u : pack_bf16x2(__uint_as_float(o[8 * e + 0]) * mul, __uint_as_float(o[8 * e + 1]) * mul);
+    v.y = zero ? 0u : pack_bf16x2(__uint_as_float(o[8 * e + 2]) * mul, __uint_as_float(o[8 * e + 3]) * mul);
+    v.z = zero ? 0u : pack_bf16x2(__uint_as_float(o[8 * e + 4]) * mul, __uint_as_float(o[8 * e + 5]) * mul);
+    v.w = zero ? 0u : pack_bf16x2(__uint_as_float(o[8 * e + 6]) * mul, __uint_as_float(o[8 * e + 7]) * mul);
+    return v;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
 // ------------------------------------------------------------------ dK, dV
+// Per query tile n the elementwise warps release P^T before they compute dS^T,
+// so the tensor pipe runs dV(n) and S^T(n + 1) while dS^T(n) is formed, and
+// dK(n), dP^T(n + 1) while P^T(n + 1) is formed.  dS^T takes P from the bf16
+// values just packed for the dV product (kept in registers).
 template <int D>
 __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dkdv_kernel(const __grid_constant__ BwdParams p)
 {
@@ -185,19 +248,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dkdv_kernel(const __gri
     const int b = bhkv / p.Hkv, g = bhkv % p.Hkv, grp = p.H / p.Hkv;
     const int kvrow = bhkv * p.S + j * p.L + tb * RA_TILE;
 
-    if (threadIdx.x == 0) {
-        mbar_init(bar(ctrl->once_full), 1);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(ctrl->st_full[s]), 1);
-            mbar_init(bar(ctrl->st_empty[s]), 1);
-        }
-        mbar_init(bar(ctrl->s_full), 1);
-        mbar_init(bar(ctrl->p_full), 128);
-        mbar_init(bar(ctrl->final_bar), 1);
-        ctrl->abort = 0;
-        fence_mbar_init();
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
+    if (threadIdx.x == 0)
+        bwd_init_barriers(ctrl);
     if (warp == 1) {
         tmem_alloc(smem_u32(&ctrl->tmem_base), BWD_TMEM_COLS);
         tmem_relinquish();
@@ -221,7 +273,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dkdv_kernel(const __gri
         uint32_t n = 0;
         bool ok = true;
         RaQWalk w;
-        w.start(j, tb, p.N, p.layout, p.causal, p.ntiles, p.H / p.Hkv);
+        w.start(j, tb, p.N, p.layout, p.causal, p.ntiles, grp);
         for (; w.valid(); w.advance(), ++n) {
             const int st = n & 1;
             if (n >= 2 && !(ok = bwait_warp(p.status, bar(ctrl->st_empty[st]), ((n >> 1) - 1) & 1, abort, tmo,
@@ -257,112 +309,144 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dkdv_kernel(const __gri
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t sK = sb + C::KV_OFF_K, sV = sb + C::KV_OFF_V;
+            const int T = dkdv_count(j, tb, p);
+            auto sQ = [&](int n) { return sb + C::KV_OFF_Q + (n & 1) * C::TILE; };
+            auto sDO = [&](int n) { return sb + C::KV_OFF_DO + (n & 1) * C::TILE; };
             bool ok = bwait(p.status, bar(ctrl->once_full), 0, abort, tmo, BS_KV_FULL);
-            uint32_t n = 0;
-            RaQWalk w;
-            w.start(j, tb, p.N, p.layout, p.causal, p.ntiles, p.H / p.Hkv);
-            for (; ok && w.valid(); w.advance(), ++n) {
-                const int st = n & 1;
-                if (!(ok = bwait(p.status, bar(ctrl->st_full[st]), (n >> 1) & 1, abort, tmo, BS_ST_FULL)))
-                    break;
-                tc_fence_after();
-                const uint32_t sQ = sb + C::KV_OFF_Q + st * C::TILE, sDO = sb + C::KV_OFF_DO + st * C::TILE;
-                issue_rows_dot<D>(tmem, sK, sQ);          // S^T = K Q^T
-                issue_rows_dot<D>(tmem + 128, sV, sDO);   // dP^T = V dO^T
-                mma_commit(bar(ctrl->s_full));
+            if (ok && T > 0) {
+                if ((ok = bwait(p.status, bar(ctrl->st_full[0]), 0, abort, tmo, BS_ST_FULL))) {
+                    tc_fence_after();
+                    issue_rows_dot<D>(tmem, sK, sQ(0));        // S^T(0) = K Q^T
+                    mma_commit(bar(ctrl->s_full[0]));
+                    issue_rows_dot<D>(tmem + 128, sV, sDO(0));  // dP^T(0) = V dO^T
+                    mma_commit(bar(ctrl->dp_full));
+                }
+            }
+            for (int n = 0; ok && n < T; ++n) {
+                const bool next = n + 1 < T;
                 if (!(ok = bwait(p.status, bar(ctrl->p_full), n & 1, abort, tmo, BS_P_FULL)))
                     break;
                 tc_fence_after();
-                issue_tmem_times_tile<D>(tmem + 256, tmem, sDO, n > 0);        // dV += P^T dO
-                issue_tmem_times_tile<D>(tmem + 256 + D, tmem + 128, sQ, n > 0);  // dK += dS^T Q
-                mma_commit(bar(ctrl->st_empty[st]));
+                issue_tmem_times_tile<D>(tmem + 256, tmem, sDO(n), n > 0);  // dV += P^T dO
+                if (next) {
+                    if (!(ok = bwait(p.status, bar(ctrl->st_full[(n + 1) & 1]), ((n + 1) >> 1) & 1, abort, tmo,
+                                     BS_ST_FULL)))
+                        break;
+                    tc_fence_after();
+                    issue_rows_dot<D>(tmem, sK, sQ(n + 1));  // S^T(n+1): P^T(n) consumed in order
+                    mma_commit(bar(ctrl->s_full[0]));
+                }
+                if (!(ok = bwait(p.status, bar(ctrl->ds_full), n & 1, abort, tmo, BS_S_FULL)))
+                    break;
+                tc_fence_after();
+                issue_tmem_times_tile<D>(tmem + 256 + D, tmem + 128, sQ(n), n > 0);  // dK += dS^T Q
+                mma_commit(bar(ctrl->st_empty[n & 1]));
+                if (next) {
+                    issue_rows_dot<D>(tmem + 128, sV, sDO(n + 1));  // dP^T(n+1): dS^T(n) consumed in order
+                    mma_commit(bar(ctrl->dp_full));
+                }
             }
             mma_commit(bar(ctrl->final_bar));
             bdrain(p.status, bar(ctrl->final_bar), 0, tmo);
         }
     } else {
         // ------------------------------------------------------------ elementwise
+        // Two warps per TMEM lane quarter: half h takes query columns
+        // [64h, 64h + 64).  Its packed P^T / dS^T land in columns [32h, 32h + 32)
+        // of the S^T / dP^T region, which for h = 1 hold half 0's inputs: the
+        // halves meet at pair[quarter] after loading and before storing.
         const int qw = warp & 3;
+        const int h = (warp - 2) >> 2;
         const int r = qw * 32 + lane;                 // key row of the tile
         const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
         const uint32_t tS = tmem + lane_off, tP = tS + 128;
         const int bl = tb * RA_TILE + r;              // key local index in block j
         const bool key_ok = bl < p.L;
         const float sl2 = p.scale_log2;
-        uint32_t n = 0;
+        const uint32_t pair = bar(ctrl->pair[qw]);
+        uint32_t n = 0, npair = 0;
         bool ok = true;
+        auto meet = [&]() -> bool {
+            tc_fence_before();
+            mbar_arrive(pair);
+            const bool met = bwait_warp(p.status, pair, npair & 1, abort, tmo, BS_S_FULL);
+            ++npair;
+            tc_fence_after();
+            return met;
+        };
         RaQWalk w;
-        w.start(j, tb, p.N, p.layout, p.causal, p.ntiles, p.H / p.Hkv);
+        w.start(j, tb, p.N, p.layout, p.causal, p.ntiles, grp);
         for (; w.valid(); w.advance(), ++n) {
-            if (!(ok = bwait_warp(p.status, bar(ctrl->s_full), n & 1, abort, tmo, BS_S_FULL)))
+            if (!(ok = bwait_warp(p.status, bar(ctrl->s_full[0]), n & 1, abort, tmo, BS_S_FULL)))
                 break;
             // the producer's lse / delta stores for this stage, made visible by
             // the stage's own barrier (complete: S^T waited for it)
             if (!(ok = bwait_warp(p.status, bar(ctrl->st_full[n & 1]), (n >> 1) & 1, abort, tmo, BS_ST_FULL)))
                 break;
             tc_fence_after();
-            const float *nl = rows + (n & 1) * 256, *dl = nl + 128;
-            // visible iff lo <= a < hi for the query local index a
+            const float *nl = rows + (n & 1) * 256 + 64 * h, *dl = nl + 128;
+            // visible iff lo <= a < L for the query local index a
             const int lo = !key_ok ? p.L : (w.cls == RA_CLS_FULL ? 0 : bl + (w.cls == RA_CLS_DIAG_EXCL ? 1 : 0));
-            const int hi = p.L;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t xs[32], xd[32];
-                tmem_ld32(tS + c * 32, xs);
-                tmem_ld32(tP + c * 32, xd);
-                tmem_wait_ld();
-                const int a0 = w.ta * RA_TILE + c * 32;
-                uint32_t pp[16], pd[16];
+            const int a0 = w.ta * RA_TILE + 64 * h;
+            uint32_t xs[64], pp[32];
+            tmem_ld64(tS + 64 * h, xs);
+            tmem_wait_ld();
+            if (!(ok = meet()))
+                break;
+            // P^T = 2^(S^T c log2e - lse log2e), masked
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const int x = c * 32 + e;
-                    float p0 = ex2_approx(fmaf(__uint_as_float(xs[e]), sl2, nl[x]));
-                    float p1 = ex2_approx(fmaf(__uint_as_float(xs[e + 1]), sl2, nl[x + 1]));
-                    p0 = (a0 + e >= lo && a0 + e < hi) ? p0 : 0.f;
-                    p1 = (a0 + e + 1 >= lo && a0 + e + 1 < hi) ? p1 : 0.f;
-                    const float d0 = p0 * (__uint_as_float(xd[e]) - dl[x]);
-                    const float d1 = p1 * (__uint_as_float(xd[e + 1]) - dl[x + 1]);
-                    pp[e >> 1] = pack_bf16x2(p0, p1);
-                    pd[e >> 1] = pack_bf16x2(d0, d1);
-                }
-                // columns [16c, 16c + 16) were read in this or an earlier chunk
-                tmem_st16(tS + c * 16, pp);
-                tmem_st16(tP + c * 16, pd);
+            for (int e = 0; e < 64; e += 2) {
+                float p0 = ex2_approx(fmaf(__uint_as_float(xs[e]), sl2, nl[e]));
+                float p1 = ex2_approx(fmaf(__uint_as_float(xs[e + 1]), sl2, nl[e + 1]));
+                p0 = (a0 + e >= lo && a0 + e < p.L) ? p0 : 0.f;
+                p1 = (a0 + e + 1 >= lo && a0 + e + 1 < p.L) ? p1 : 0.f;
+                pp[e >> 1] = pack_bf16x2(p0, p1);
             }
+            tmem_st32(tS + 32 * h, pp);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(ctrl->p_full));
+            // dS^T = P^T (dP^T - delta), P^T as packed for the dV product
+            if (!(ok = bwait_warp(p.status, bar(ctrl->dp_full), n & 1, abort, tmo, BS_S_FULL)))
+                break;
+            tc_fence_after();
+            uint32_t xd[64], pd[32];
+            tmem_ld64(tP + 64 * h, xd);
+            tmem_wait_ld();
+            if (!(ok = meet()))
+                break;
+#pragma unroll
+            for (int e = 0; e < 64; e += 2) {
+                const uint32_t pk = pp[e >> 1];
+                pd[e >> 1] = pack_bf16x2(bf16_lo(pk) * (__uint_as_float(xd[e]) - dl[e]),
+                                         bf16_hi(pk) * (__uint_as_float(xd[e + 1]) - dl[e + 1]));
+            }
+            tmem_st32(tP + 32 * h, pd);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(ctrl->ds_full));
         }
         // ------------------------------------------------------------ epilogue
+        // half 0 writes dV, half 1 dK
         if (ok)
             ok = bwait_warp(p.status, bar(ctrl->final_bar), 0, abort, tmo, BS_FINAL);
         if (ok) {
             tc_fence_after();
             const long long orow = (long long)kvrow + r;
+            __nv_bfloat16 *dst = h == 0 ? p.dv : p.dk;
+            const float mul = h == 0 ? 1.f : p.scale;
 #pragma unroll 1
-            for (int which = 0; which < 2; ++which) {
-                __nv_bfloat16 *dst = which == 0 ? p.dv : p.dk;
-                const float mul = which == 0 ? 1.f : p.scale;
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    __syncwarp();
-                    tmem_ld32(tS + 256 + which * D + c * 32, o);
-                    tmem_wait_ld();
-                    if (!key_ok)
-                        continue;
-                    uint4 *out = reinterpret_cast<uint4 *>(dst + orow * D + c * 32);
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                __syncwarp();
+                tmem_ld32(tS + 256 + h * D + c * 32, o);
+                tmem_wait_ld();
+                if (!key_ok)
+                    continue;
+                uint4 *out = reinterpret_cast<uint4 *>(dst + orow * D + c * 32);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        uint4 v;
-                        const bool z = (n == 0);  // no query tile met this key tile
-                        v.x = z ? 0u : pack_bf16x2(__uint_as_float(o[8 * e + 0]) * mul, __uint_as_float(o[8 * e + 1]) * mul);
-                        v.y = z ? 0u : pack_bf16x2(__uint_as_float(o[8 * e + 2]) * mul, __uint_as_float(o[8 * e + 3]) * mul);
-                        v.z = z ? 0u : pack_bf16x2(__uint_as_float(o[8 * e + 4]) * mul, __uint_as_float(o[8 * e + 5]) * mul);
-                        v.w = z ? 0u : pack_bf16x2(__uint_as_float(o[8 * e + 6]) * mul, __uint_as_float(o[8 * e + 7]) * mul);
-                        out[e] = v;
-                    }
-                }
+                for (int e = 0; e < 4; ++e)
+                    out[e] = pack8(o, e, mul, n == 0);  // n == 0: no query tile met this key tile
             }
         }
     }
@@ -377,6 +461,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dkdv_kernel(const __gri
 }
 
 // ------------------------------------------------------------------ dQ
+// Two S buffers (columns [0,128) and [384,512)): S(n + 2) is computed while
+// the elementwise warps work on tile n + 1, and dP(n + 1) is issued before
+// dQ(n), so the elementwise work of one key tile waits only for its dP.
 template <int D>
 __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dq_kernel(const __grid_constant__ BwdParams p)
 {
@@ -395,19 +482,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dq_kernel(const __grid_
     const int kvbh = b * p.Hkv + h / (p.H / p.Hkv);
     const int qrow = bh * p.S + i * p.L + ta * RA_TILE;
 
-    if (threadIdx.x == 0) {
-        mbar_init(bar(ctrl->once_full), 1);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(ctrl->st_full[s]), 1);
-            mbar_init(bar(ctrl->st_empty[s]), 1);
-        }
-        mbar_init(bar(ctrl->s_full), 1);
-        mbar_init(bar(ctrl->p_full), 128);
-        mbar_init(bar(ctrl->final_bar), 1);
-        ctrl->abort = 0;
-        fence_mbar_init();
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
+    if (threadIdx.x == 0)
+        bwd_init_barriers(ctrl);
     if (warp == 1) {
         tmem_alloc(smem_u32(&ctrl->tmem_base), BWD_TMEM_COLS);
         tmem_relinquish();
@@ -432,7 +508,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dq_kernel(const __grid_
             w.start(i, ta, p.N, p.layout, p.causal, p.ntiles);
             for (; w.valid(); w.advance(), ++n) {
                 const int st = n & 1;
-                if (n >= 2 && !(ok = bwait(p.status, bar(ctrl->st_empty[st]), ((n >> 1) - 1) & 1, abort, tmo, BS_KV_EMPTY)))
+                if (n >= 2 && !(ok = bwait(p.status, bar(ctrl->st_empty[st]), ((n >> 1) - 1) & 1, abort, tmo,
+                                           BS_KV_EMPTY)))
                     break;
                 const int row = kvbh * p.S + w.j * p.L + w.tb * RA_TILE;
                 mbar_arrive_expect_tx(bar(ctrl->st_full[st]), 2 * C::TILE);
@@ -447,67 +524,98 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dq_kernel(const __grid_
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t sQ = sb + C::Q_OFF_Q, sDO = sb + C::Q_OFF_DO;
+            const int T = dq_count(i, ta, p);
+            auto sK = [&](int n) { return sb + C::Q_OFF_K + (n & 1) * C::TILE; };
+            auto sV = [&](int n) { return sb + C::Q_OFF_V + (n & 1) * C::TILE; };
             bool ok = bwait(p.status, bar(ctrl->once_full), 0, abort, tmo, BS_Q_FULL);
-            uint32_t n = 0;
-            RaKWalk w;
-            w.start(i, ta, p.N, p.layout, p.causal, p.ntiles);
-            for (; ok && w.valid(); w.advance(), ++n) {
-                const int st = n & 1;
-                if (!(ok = bwait(p.status, bar(ctrl->st_full[st]), (n >> 1) & 1, abort, tmo, BS_ST_FULL)))
+            // S(0), dP(0), S(1)
+            for (int n = 0; ok && n < 2 && n < T; ++n) {
+                if (!(ok = bwait(p.status, bar(ctrl->st_full[n]), 0, abort, tmo, BS_ST_FULL)))
                     break;
                 tc_fence_after();
-                const uint32_t sK = sb + C::Q_OFF_K + st * C::TILE, sV = sb + C::Q_OFF_V + st * C::TILE;
-                issue_rows_dot<D>(tmem, sQ, sK);          // S = Q K^T
-                issue_rows_dot<D>(tmem + 128, sDO, sV);   // dP = dO V^T
-                mma_commit(bar(ctrl->s_full));
+                issue_rows_dot<D>(tmem + (n ? 384u : 0u), sQ, sK(n));
+                mma_commit(bar(ctrl->s_full[n]));
+                if (n == 0) {
+                    issue_rows_dot<D>(tmem + 128, sDO, sV(0));
+                    mma_commit(bar(ctrl->dp_full));
+                }
+            }
+            for (int n = 0; ok && n < T; ++n) {
                 if (!(ok = bwait(p.status, bar(ctrl->p_full), n & 1, abort, tmo, BS_P_FULL)))
                     break;
                 tc_fence_after();
-                issue_tmem_times_tile<D>(tmem + 256, tmem, sK, n > 0);  // dQ += dS K
-                mma_commit(bar(ctrl->st_empty[st]));
+                if (n + 1 < T) {
+                    issue_rows_dot<D>(tmem + 128, sDO, sV(n + 1));  // dP(n+1): dP(n) was read
+                    mma_commit(bar(ctrl->dp_full));
+                }
+                issue_tmem_times_tile<D>(tmem + 256, tmem + ((n & 1) ? 384u : 0u), sK(n), n > 0);  // dQ += dS K
+                mma_commit(bar(ctrl->st_empty[n & 1]));
+                if (n + 2 < T) {
+                    if (!(ok = bwait(p.status, bar(ctrl->st_full[n & 1]), ((n + 2) >> 1) & 1, abort, tmo,
+                                     BS_ST_FULL)))
+                        break;
+                    tc_fence_after();
+                    issue_rows_dot<D>(tmem + ((n & 1) ? 384u : 0u), sQ, sK(n + 2));  // dS(n) consumed in order
+                    mma_commit(bar(ctrl->s_full[n & 1]));
+                }
             }
             mma_commit(bar(ctrl->final_bar));
             bdrain(p.status, bar(ctrl->final_bar), 0, tmo);
         }
     } else {
+        // Two warps per TMEM lane quarter, half h on key columns [64h, 64h + 64);
+        // packed dS goes to columns [32h, 32h + 32) of the S buffer, which for
+        // h = 1 still hold half 0's scores until the halves meet at pair[quarter].
         const int qw = warp & 3;
+        const int h = (warp - 2) >> 2;
         const int r = qw * 32 + lane;
         const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
-        const uint32_t tS = tmem + lane_off, tP = tS + 128;
+        const uint32_t tP = tmem + lane_off + 128;
         const int a = ta * RA_TILE + r;
         const bool row_ok = a < p.L;
         const long long grow = (long long)qrow + r;
         const float nl = row_ok ? -p.lse[grow] * LOG2E : 0.f;
         const float dl = row_ok ? p.delta[grow] : 0.f;
         const float sl2 = p.scale_log2;
+        const uint32_t pair = bar(ctrl->pair[qw]);
         uint32_t n = 0;
         bool ok = true;
         RaKWalk w;
         w.start(i, ta, p.N, p.layout, p.causal, p.ntiles);
         for (; w.valid(); w.advance(), ++n) {
-            if (!(ok = bwait_warp(p.status, bar(ctrl->s_full), n & 1, abort, tmo, BS_S_FULL)))
+            const uint32_t tS = tmem + lane_off + ((n & 1) ? 384u : 0u);
+            if (!(ok = bwait_warp(p.status, bar(ctrl->s_full[n & 1]), (n >> 1) & 1, abort, tmo, BS_S_FULL)))
+                break;
+            if (!(ok = bwait_warp(p.status, bar(ctrl->dp_full), n & 1, abort, tmo, BS_S_FULL)))
                 break;
             tc_fence_after();
-            const int lim = row_ok ? ra_key_limit(w.cls, a, p.L) - w.tb * RA_TILE : 0;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t xs[32], xd[32];
-                tmem_ld32(tS + c * 32, xs);
-                tmem_ld32(tP + c * 32, xd);
+            const int lim = (row_ok ? ra_key_limit(w.cls, a, p.L) - w.tb * RA_TILE : 0) - 64 * h;
+            uint32_t xs[64];
+            tmem_ld64(tS + 64 * h, xs);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(pair);
+            if (!(ok = bwait_warp(p.status, pair, n & 1, abort, tmo, BS_S_FULL)))
+                break;
+            tc_fence_after();
+            uint32_t pd[32];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t xd[32];
+                tmem_ld32(tP + 64 * h + 32 * c, xd);
                 tmem_wait_ld();
-                uint32_t pd[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    const int x = c * 32 + e;
-                    float p0 = ex2_approx(fmaf(__uint_as_float(xs[e]), sl2, nl));
-                    float p1 = ex2_approx(fmaf(__uint_as_float(xs[e + 1]), sl2, nl));
+                    const int x = 32 * c + e;
+                    float p0 = ex2_approx(fmaf(__uint_as_float(xs[x]), sl2, nl));
+                    float p1 = ex2_approx(fmaf(__uint_as_float(xs[x + 1]), sl2, nl));
                     p0 = x < lim ? p0 : 0.f;
                     p1 = x + 1 < lim ? p1 : 0.f;
-                    pd[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(xd[e]) - dl),
+                    pd[x >> 1] = pack_bf16x2(p0 * (__uint_as_float(xd[e]) - dl),
                                              p1 * (__uint_as_float(xd[e + 1]) - dl));
                 }
-                tmem_st16(tS + c * 16, pd);
             }
+            tmem_st32(tS + 32 * h, pd);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(ctrl->p_full));
@@ -517,25 +625,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dq_kernel(const __grid_
         if (ok) {
             tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < D / 64; ++c) {
                 uint32_t o[32];
                 __syncwarp();
-                tmem_ld32(tS + 256 + c * 32, o);
+                tmem_ld32(tmem + lane_off + 256 + h * (D / 2) + c * 32, o);
                 tmem_wait_ld();
                 if (!row_ok)
                     continue;
-                uint4 *out = reinterpret_cast<uint4 *>(p.dq + grow * D + c * 32);
-                const float mul = p.scale;
-                const bool z = (n == 0);
+                uint4 *out = reinterpret_cast<uint4 *>(p.dq + grow * D + h * (D / 2) + c * 32);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    uint4 v;
-                    v.x = z ? 0u : pack_bf16x2(__uint_as_float(o[8 * e + 0]) * mul, __uint_as_float(o[8 * e + 1]) * mul);
-                    v.y = z ? 0u : pack_bf16x2(__uint_as_float(o[8 * e + 2]) * mul, __uint_as_float(o[8 * e + 3]) * mul);
-                    v.z = z ? 0u : pack_bf16x2(__uint_as_float(o[8 * e + 4]) * mul, __uint_as_float(o[8 * e + 5]) * mul);
-                    v.w = z ? 0u : pack_bf16x2(__uint_as_float(o[8 * e + 6]) * mul, __uint_as_float(o[8 * e + 7]) * mul);
-                    out[e] = v;
-                }
+                for (int e = 0; e < 4; ++e)
+                    out[e] = pack8(o, e, p.scale, n == 0);
             }
         }
     }
