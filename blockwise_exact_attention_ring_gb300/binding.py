@@ -59,6 +59,7 @@ def lib():
     L.ra_all_to_all.argtypes = [vp, vp] + [i] * 7 + [vp]
     L.ra_backward.argtypes = [vp] * 9 + [i] * 8 + [vp]
     L.ra_backward_ws.argtypes = [vp] * 9 + [i] * 8 + [vp, sz, vp]
+    L.ra_backward_f32.argtypes = [vp] * 9 + [i] * 8 + [vp]
     L.ra_backward_workspace_bytes.argtypes = [i] * 8
     L.ra_backward_workspace_bytes.restype = sz
     L.ra_backward_tile_pairs.argtypes = [i] * 8 + [vp, ll]
@@ -87,7 +88,7 @@ def lib():
     L.ra_schedule_stats.restype = ll
     for fn in ("ra_forward", "ra_forward_f32", "ra_forward_noalloc", "ra_forward_ws",
                "ra_forward_rank_major", "ra_forward_block", "ra_all_to_all", "ra_forward_ulysses",
-               "ra_backward", "ra_backward_ws", "ra_permute", "ra_merge", "ra_check"):
+               "ra_backward", "ra_backward_ws", "ra_backward_f32", "ra_permute", "ra_merge", "ra_check"):
         getattr(L, fn).restype = i
     _lib = L
     return L
@@ -271,21 +272,24 @@ def forward_block(q, k, v, out_s, lse_s, n_blocks, rank, step, layout="contiguou
 def backward(q, k, v, out, lse, dout, n_blocks: int, layout: str = "contiguous", causal: bool = False,
              workspace=None, stream=None):
     """Gradients (dq, dk, dv) of sum(dout * out) for (out, lse) = forward(q, k,
-    v, ...) with the same n_blocks, layout and causal (ra_backward / ra_backward_ws).
-    bf16 CUDA tensors in natural token order; lse fp32 [B,H,S]."""
+    v, ...) with the same n_blocks, layout and causal (ra_backward / ra_backward_ws
+    for bf16, ra_backward_f32 for fp32).  CUDA tensors in natural token order;
+    lse fp32 [B,H,S]."""
     B, H, Hkv, S, d = _dims(q, k, v)
-    if q.dtype != torch.bfloat16:
-        raise ValueError("the backward pass takes bf16 tensors")
     for t, shape in ((out, q.shape), (dout, q.shape)):
-        if t.shape != shape or t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
-            raise ValueError("out and dout must be contiguous bf16 CUDA tensors shaped like q")
+        if t.shape != shape or t.dtype != q.dtype or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("out and dout must be contiguous CUDA tensors shaped like q, of q's dtype")
     if lse.shape != (B, H, S) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 [B,H,S] tensor")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     L = lib()
     args = [_p(q), _p(k), _p(v), _p(out), _p(lse), _p(dout), _p(dq), _p(dk), _p(dv), B, H, Hkv, S, d,
             n_blocks, LAYOUTS[layout], int(bool(causal))]
-    if workspace is None:
+    if q.dtype == torch.float32:
+        if workspace is not None:
+            raise ValueError("the fp32 backward allocates its own scratch")
+        _check(L.ra_backward_f32(*args, _stream(stream)), "ra_backward_f32")
+    elif workspace is None:
         _check(L.ra_backward(*args, _stream(stream)), "ra_backward")
     else:
         _check(L.ra_backward_ws(*args, _p(workspace), workspace.numel() * workspace.element_size(),

@@ -454,7 +454,7 @@ BwdWs bwd_ws_layout(const Problem &p)
     };
     w.delta = take(p.rows() * 4);
     if (p.layout == RA_LAYOUT_STRIPED) {
-        const size_t qb = p.q_elems() * 2, kvb = p.kv_elems() * 2;
+        const size_t qb = p.q_elems() * p.esz(), kvb = p.kv_elems() * p.esz();
         w.q = take(qb), w.k = take(kvb), w.v = take(kvb), w.out = take(qb), w.dout = take(qb);
         w.lse = take(p.rows() * 4);
         w.dq = take(qb), w.dk = take(kvb), w.dv = take(kvb);
@@ -476,7 +476,7 @@ ra_status backward_impl(const Problem &p, const void *q, const void *k, const vo
     for (const void *x : all)
         if (!aligned16(x))
             return RA_ERR_INVALID_ARG;
-    const size_t qb = p.q_elems() * 2, kvb = p.kv_elems() * 2, lb = p.rows() * 4;
+    const size_t qb = p.q_elems() * p.esz(), kvb = p.kv_elems() * p.esz(), lb = p.rows() * 4;
     const size_t sizes[] = {qb, kvb, kvb, qb, lb, qb, qb, kvb, kvb};
     // the three gradients must not overlap any input or each other
     for (int o = 6; o < 9; ++o)
@@ -489,7 +489,7 @@ ra_status backward_impl(const Problem &p, const void *q, const void *k, const vo
     const int sm = sm_count_current();
     char *base = static_cast<char *>(ws);
     const bool striped = p.layout == RA_LAYOUT_STRIPED;
-    const long long row = (long long)p.d * 2;
+    const long long row = (long long)p.d * (long long)p.esz();
     const long long qrows = (long long)p.B * p.H * p.S, kvrows = (long long)p.B * p.Hkv * p.S;
     ra::BwdLaunch a{};
     a.q = q, a.k = k, a.v = v, a.out = out, a.dout = dout, a.lse = lse;
@@ -513,7 +513,11 @@ ra_status backward_impl(const Problem &p, const void *q, const void *k, const vo
     a.layout = p.layout, a.causal = p.causal;
     a.timeout_ns = g_timeout_ns;
     count_launch(3);
-    if (ra::launch_bwd(a, st) != cudaSuccess)
+    if (p.dtype == RA_DTYPE_F32)
+        ra::launch_bwd_f32(a, st);
+    else if (ra::launch_bwd(a, st) != cudaSuccess)
+        return RA_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess)
         return RA_ERR_CUDA;
     if (striped) {
         ra::launch_permute(base + w.dq, dq, qrows, p.S, p.N, row, 1, sm, st);
@@ -727,6 +731,34 @@ ra_status ra_backward_ws(const void *q, const void *k, const void *v, const void
 {
     const Problem p{B, H, Hkv, S, d, n_blocks, layout, causal, RA_DTYPE_BF16, RA_MODE_FUSED};
     return backward_impl(p, q, k, v, out, lse, dout, dq, dk, dv, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+namespace {
+ra_status backward_alloc(const Problem &p, const void *q, const void *k, const void *v, const void *out,
+                         const float *lse, const void *dout, void *dq, void *dk, void *dv, cudaStream_t st)
+{
+    ra_status rs = check_problem(p);
+    if (rs != RA_OK)
+        return rs;
+    const size_t bytes = bwd_ws_layout(p).total;
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, bytes, st) != cudaSuccess) {
+        cudaGetLastError();
+        return RA_ERR_NO_MEMORY;
+    }
+    rs = backward_impl(p, q, k, v, out, lse, dout, dq, dk, dv, ws, bytes, st);
+    if (cudaFreeAsync(ws, st) != cudaSuccess && rs == RA_OK)
+        rs = RA_ERR_CUDA;
+    return rs;
+}
+}  // namespace
+
+ra_status ra_backward_f32(const float *q, const float *k, const float *v, const float *out, const float *lse,
+                          const float *dout, float *dq, float *dk, float *dv, int B, int H, int Hkv, int S, int d,
+                          int n_blocks, int layout, int causal, ra_stream_t stream)
+{
+    const Problem p{B, H, Hkv, S, d, n_blocks, layout, causal, RA_DTYPE_F32, RA_MODE_FUSED};
+    return backward_alloc(p, q, k, v, out, lse, dout, dq, dk, dv, (cudaStream_t)stream);
 }
 
 ra_status ra_backward(const void *q, const void *k, const void *v, const void *out, const float *lse,

@@ -58,12 +58,14 @@ struct BwdLaunch {
     const void *q, *k, *v, *out, *dout;
     const float *lse;
     float *delta;                // written
-    void *dq, *dk, *dv;          // written, bf16
+    void *dq, *dk, *dv;          // written, bf16 (fp32 for launch_bwd_f32)
     int B, H, Hkv, S, d, N;
     int layout, causal;
     unsigned long long timeout_ns;
 };
 cudaError_t launch_bwd(const BwdLaunch &a, cudaStream_t st);
+// The same pass in fp32 on the SIMT cores (any d <= 256): delta, dQ, dK/dV.
+void launch_bwd_f32(const BwdLaunch &a, cudaStream_t st);
 
 // Device address of the library's status word on the current device (the
 // word ra_check reads); kernels in other translation units get it as a

@@ -261,6 +261,14 @@ ra_status ra_backward(const void *q, const void *k, const void *v, const void *o
                       int B, int H, int Hkv, int S, int d, int n_blocks, int layout,
                       int causal, ra_stream_t stream);
 
+/* ra_backward_f32 - ra_backward with every tensor in fp32 (exact SIMT path,
+ * no tensor cores, no bf16 rounding; any 1 <= d <= 256), for checks at fp32
+ * precision.  Same arguments and error rules as ra_backward. */
+ra_status ra_backward_f32(const float *q, const float *k, const float *v, const float *out,
+                          const float *lse, const float *dout, float *dq, float *dk, float *dv,
+                          int B, int H, int Hkv, int S, int d, int n_blocks, int layout,
+                          int causal, ra_stream_t stream);
+
 /* ra_backward_workspace_bytes - scratch ra_backward_ws needs (delta per row;
  * for the striped layout, rank-major copies of the inputs and gradients);
  * 0 for an invalid request. */

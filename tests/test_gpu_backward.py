@@ -114,6 +114,36 @@ def test_backward_workload_32k_properties_and_sampled_rows():
     assert dk_sum.abs().max().item() <= 1e-2 * dk.double().abs().sum(dim=2).max().item()
 
 
+F32_CASES = [
+    # B, H, Hkv, S, d, N, layout, causal
+    (1, 1, 1, 32, 16, 4, "contiguous", False),   # the pages' 4-device example shape
+    (1, 2, 1, 96, 32, 3, "striped", True),
+    (2, 2, 2, 64, 16, 4, "contiguous", True),
+    (1, 4, 2, 128, 64, 2, "contiguous", False),
+    (1, 3, 1, 90, 40, 3, "striped", False),      # d not a multiple of 32
+]
+
+
+@pytest.mark.parametrize("case", F32_CASES, ids=lambda c: "B{}H{}kv{}S{}d{}N{}-{}-{}".format(*c))
+def test_backward_f32_exact(case):
+    """The fp32 path (ra_backward_f32) against the fp64 oracle at fp32
+    precision: max error <= 1e-5 of max(1, max |ref|)."""
+    B, H, Hkv, S, d, N, layout, causal = case
+    if (B, H, S, d) == (1, 1, 32, 16):
+        q, k, v = inputs.page_example_qkv()
+    else:
+        q, k, v = inputs.make_qkv(B, H, Hkv, S, d, seed=S * d, dtype=torch.float32)
+    g = torch.Generator().manual_seed(S + d)
+    dout = torch.randn(B, H, S, d, generator=g)
+    qd, kd, vd, dod = (t.cuda().contiguous() for t in (q, k, v, dout))
+    out, lse = ra.forward(qd, kd, vd, n_blocks=N, layout=layout, causal=causal)
+    grads = ra.backward(qd, kd, vd, out, lse, dod, N, layout=layout, causal=causal)
+    ra.check()
+    for name, got, ref in zip(("dq", "dk", "dv"), grads, attention_backward(q, k, v, dout, causal)):
+        err = np.abs(got.cpu().double().numpy() - ref).max()
+        assert err <= 1e-5 * max(1.0, np.abs(ref).max()), f"{name}: {err:.3g}"
+
+
 def test_backward_rejects_bad_arguments():
     q, k, v = (t.cuda() for t in inputs.make_qkv(1, 2, 1, 256, 64, seed=1))
     out, lse = ra.forward(q, k, v, n_blocks=2, causal=True)
