@@ -16,6 +16,9 @@ Contents
                    sequence shards of n devices [n, B, Hn, S/n, d].
 ``heads_of``       what each device holds after the Ulysses all-to-all: all
                    tokens of its heads, [n, B, Hn/n, S, d].
+``backward.attention_backward`` / ``backward.dq_rows``  fp64 gradients of
+                   exact attention (oracle/backward.py), pinned in
+                   tests/test_oracle_backward.py.
 
 Sources (web pages on ring attention):
   * "Ring Attention" glossary page (ultralytics.com/tr), section
