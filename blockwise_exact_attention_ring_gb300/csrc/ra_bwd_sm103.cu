@@ -69,12 +69,14 @@ struct BwdCfg {
     static constexpr int KV_OFF_ROWS = 6 * TILE;           // [stage][nl | dl][128] floats
     static constexpr int KV_OFF_CTRL = KV_OFF_ROWS + 2 * 2 * 128 * 4;
     static constexpr int KV_SMEM = KV_OFF_CTRL + 256 + 1024;
-    // dQ kernel: Q, dO once; K and V in two stages
+    // dQ kernel: Q, dO once; K in three stages (held until dQ), V in two
+    // (free once dP has read it)
+    static constexpr int Q_KST = 3;
     static constexpr int Q_OFF_Q = 0;
     static constexpr int Q_OFF_DO = TILE;
     static constexpr int Q_OFF_K = 2 * TILE;
-    static constexpr int Q_OFF_V = 4 * TILE;
-    static constexpr int Q_OFF_CTRL = 6 * TILE;
+    static constexpr int Q_OFF_V = (2 + Q_KST) * TILE;
+    static constexpr int Q_OFF_CTRL = (4 + Q_KST) * TILE;
     static constexpr int Q_SMEM = Q_OFF_CTRL + 256 + 1024;
     // Both kernels allocate all 512 TMEM columns: ask for enough shared
     // memory that a second CTA never lands on the same SM (it would block in
@@ -86,7 +88,8 @@ struct BwdCfg {
 
 struct BwdCtrl {
     uint64_t once_full;            // K, V (dK/dV) or Q, dO (dQ)
-    uint64_t st_full[2], st_empty[2];
+    uint64_t st_full[2], st_empty[2];  // dK/dV: Q, dO stages; dQ: V stages
+    uint64_t kf[3], ke[3];         // dQ: K stages
     uint64_t s_full[2];            // S (per S buffer)
     uint64_t dp_full;              // dP
     uint64_t p_full;               // dK/dV: P^T written; dQ: dS written (256 arrivals)
@@ -96,6 +99,8 @@ struct BwdCtrl {
     uint32_t tmem_base;
     int abort;
 };
+
+static_assert(sizeof(BwdCtrl) <= 256, "control block");
 
 struct BwdParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;
@@ -129,14 +134,15 @@ __device__ __forceinline__ void bdrain(unsigned int *st, uint32_t bar, uint32_t 
     mbar_wait(bar, parity, &never, tmo, st, BS_DRAIN);
 }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
+// Bring one [128 rows][D] tile into L2 ahead of its TMA load (no shared
+// memory, no barrier).
+template <int D>
+__device__ __forceinline__ void bprefetch_tile(const CUtensorMap *tm, int row)
 {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-                 "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
-                 ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
-                   "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
-                   "r"(r[13]), "r"(r[14]), "r"(r[15])
-                 : "memory");
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h)
+        asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                     ::"l"(tm), "r"(h * 64), "r"(row) : "memory");
 }
 
 template <int D>
@@ -200,6 +206,10 @@ __device__ __forceinline__ void bwd_init_barriers(BwdCtrl *ctrl)
         mbar_init(smem_u32(&ctrl->st_full[s]), 1);
         mbar_init(smem_u32(&ctrl->st_empty[s]), 1);
         mbar_init(smem_u32(&ctrl->s_full[s]), 1);
+    }
+    for (int s = 0; s < 3; ++s) {
+        mbar_init(smem_u32(&ctrl->kf[s]), 1);
+        mbar_init(smem_u32(&ctrl->ke[s]), 1);
     }
     mbar_init(smem_u32(&ctrl->dp_full), 1);
     mbar_init(smem_u32(&ctrl->p_full), BWD_EW);
@@ -276,11 +286,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dkdv_kernel(const __gri
         w.start(j, tb, p.N, p.layout, p.causal, p.ntiles, grp);
         for (; w.valid(); w.advance(), ++n) {
             const int st = n & 1;
-            if (n >= 2 && !(ok = bwait_warp(p.status, bar(ctrl->st_empty[st]), ((n >> 1) - 1) & 1, abort, tmo,
-                                            BS_ST_EMPTY)))
-                break;
             const int bh = b * p.H + g * grp + w.hh;
             const long long row0 = (long long)bh * p.S + (long long)w.i * p.L + w.ta * RA_TILE;
+            if (n >= 2) {
+                if (lane == 0) {
+                    // the stage frees only after dK(n - 2): have the tiles in L2 by then
+                    bprefetch_tile<D>(&p.tm_q, (int)row0);
+                    bprefetch_tile<D>(&p.tm_do, (int)row0);
+                }
+                if (!(ok = bwait_warp(p.status, bar(ctrl->st_empty[st]), ((n >> 1) - 1) & 1, abort, tmo,
+                                      BS_ST_EMPTY)))
+                    break;
+            }
             float *nl = rows + st * 256, *dl = nl + 128;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -506,38 +523,65 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dq_kernel(const __grid_
             bool ok = true;
             RaKWalk w;
             w.start(i, ta, p.N, p.layout, p.causal, p.ntiles);
+            uint32_t nk = 0, nv = 0;  // K and V loads issued
             for (; w.valid(); w.advance(), ++n) {
-                const int st = n & 1;
-                if (n >= 2 && !(ok = bwait(p.status, bar(ctrl->st_empty[st]), ((n >> 1) - 1) & 1, abort, tmo,
-                                           BS_KV_EMPTY)))
-                    break;
+                const int ks = n % C::Q_KST, vs = n & 1;
                 const int row = kvbh * p.S + w.j * p.L + w.tb * RA_TILE;
-                mbar_arrive_expect_tx(bar(ctrl->st_full[st]), 2 * C::TILE);
-                bload_tile<D>(sb + C::Q_OFF_K + st * C::TILE, &p.tm_k, row, bar(ctrl->st_full[st]), pol_kv);
-                bload_tile<D>(sb + C::Q_OFF_V + st * C::TILE, &p.tm_v, row, bar(ctrl->st_full[st]), pol_kv);
+                if (n >= (uint32_t)C::Q_KST) {
+                    // K's stage frees after dQ(n - 3): have the tile in L2 by then
+                    bprefetch_tile<D>(&p.tm_k, row);
+                    if (!(ok = bwait(p.status, bar(ctrl->ke[ks]), (n / C::Q_KST - 1) & 1, abort, tmo,
+                                     BS_KV_EMPTY)))
+                        break;
+                }
+                mbar_arrive_expect_tx(bar(ctrl->kf[ks]), C::TILE);
+                bload_tile<D>(sb + C::Q_OFF_K + ks * C::TILE, &p.tm_k, row, bar(ctrl->kf[ks]), pol_kv);
+                ++nk;
+                if (n >= 2) {
+                    // V's stage frees once dP(n - 2) has read it
+                    bprefetch_tile<D>(&p.tm_v, row);
+                    if (!(ok = bwait(p.status, bar(ctrl->st_empty[vs]), ((n >> 1) - 1) & 1, abort, tmo,
+                                     BS_KV_EMPTY)))
+                        break;
+                }
+                mbar_arrive_expect_tx(bar(ctrl->st_full[vs]), C::TILE);
+                bload_tile<D>(sb + C::Q_OFF_V + vs * C::TILE, &p.tm_v, row, bar(ctrl->st_full[vs]), pol_kv);
+                ++nv;
             }
+            // every issued copy lands before shared memory is released
             bdrain(p.status, bar(ctrl->once_full), 0, tmo);
-            for (uint32_t m = n > 2 ? n - 2 : 0; m < n; ++m)
+            for (uint32_t m = nk > (uint32_t)C::Q_KST ? nk - C::Q_KST : 0; m < nk; ++m)
+                bdrain(p.status, bar(ctrl->kf[m % C::Q_KST]), (m / C::Q_KST) & 1, tmo);
+            for (uint32_t m = nv > 2 ? nv - 2 : 0; m < nv; ++m)
                 bdrain(p.status, bar(ctrl->st_full[m & 1]), (m >> 1) & 1, tmo);
-            (void)ok;
         }
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t sQ = sb + C::Q_OFF_Q, sDO = sb + C::Q_OFF_DO;
             const int T = dq_count(i, ta, p);
-            auto sK = [&](int n) { return sb + C::Q_OFF_K + (n & 1) * C::TILE; };
+            auto sK = [&](int n) { return sb + C::Q_OFF_K + (n % C::Q_KST) * C::TILE; };
             auto sV = [&](int n) { return sb + C::Q_OFF_V + (n & 1) * C::TILE; };
+            auto wait_k = [&](int n) {
+                return bwait(p.status, bar(ctrl->kf[n % C::Q_KST]), (n / C::Q_KST) & 1, abort, tmo, BS_ST_FULL);
+            };
+            auto wait_v = [&](int n) {
+                return bwait(p.status, bar(ctrl->st_full[n & 1]), (n >> 1) & 1, abort, tmo, BS_ST_FULL);
+            };
             bool ok = bwait(p.status, bar(ctrl->once_full), 0, abort, tmo, BS_Q_FULL);
             // S(0), dP(0), S(1)
             for (int n = 0; ok && n < 2 && n < T; ++n) {
-                if (!(ok = bwait(p.status, bar(ctrl->st_full[n]), 0, abort, tmo, BS_ST_FULL)))
+                if (!(ok = wait_k(n)))
                     break;
                 tc_fence_after();
                 issue_rows_dot<D>(tmem + (n ? 384u : 0u), sQ, sK(n));
                 mma_commit(bar(ctrl->s_full[n]));
                 if (n == 0) {
+                    if (!(ok = wait_v(0)))
+                        break;
+                    tc_fence_after();
                     issue_rows_dot<D>(tmem + 128, sDO, sV(0));
                     mma_commit(bar(ctrl->dp_full));
+                    mma_commit(bar(ctrl->st_empty[0]));
                 }
             }
             for (int n = 0; ok && n < T; ++n) {
@@ -545,14 +589,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dq_kernel(const __grid_
                     break;
                 tc_fence_after();
                 if (n + 1 < T) {
+                    if (!(ok = wait_v(n + 1)))
+                        break;
+                    tc_fence_after();
                     issue_rows_dot<D>(tmem + 128, sDO, sV(n + 1));  // dP(n+1): dP(n) was read
                     mma_commit(bar(ctrl->dp_full));
+                    mma_commit(bar(ctrl->st_empty[(n + 1) & 1]));
                 }
                 issue_tmem_times_tile<D>(tmem + 256, tmem + ((n & 1) ? 384u : 0u), sK(n), n > 0);  // dQ += dS K
-                mma_commit(bar(ctrl->st_empty[n & 1]));
+                mma_commit(bar(ctrl->ke[n % C::Q_KST]));
                 if (n + 2 < T) {
-                    if (!(ok = bwait(p.status, bar(ctrl->st_full[n & 1]), ((n + 2) >> 1) & 1, abort, tmo,
-                                     BS_ST_FULL)))
+                    if (!(ok = wait_k(n + 2)))
                         break;
                     tc_fence_after();
                     issue_rows_dot<D>(tmem + ((n & 1) ? 384u : 0u), sQ, sK(n + 2));  // dS(n) consumed in order
