@@ -410,14 +410,27 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dkdv_kernel(const __gri
             tmem_wait_ld();
             if (!(ok = meet()))
                 break;
-            // P^T = 2^(S^T c log2e - lse log2e), masked
+            // P^T = 2^(S^T c log2e - lse log2e), masked where some query of the
+            // warp's half-tile does not see the warp's keys
+            const float2 sl2x2 = make_float2(sl2, sl2);
+            const float2 *nl2 = reinterpret_cast<const float2 *>(nl);
+            if (__all_sync(0xffffffffu, lo <= a0 && a0 + 64 <= p.L)) {
 #pragma unroll
-            for (int e = 0; e < 64; e += 2) {
-                float p0 = ex2_approx(fmaf(__uint_as_float(xs[e]), sl2, nl[e]));
-                float p1 = ex2_approx(fmaf(__uint_as_float(xs[e + 1]), sl2, nl[e + 1]));
-                p0 = (a0 + e >= lo && a0 + e < p.L) ? p0 : 0.f;
-                p1 = (a0 + e + 1 >= lo && a0 + e + 1 < p.L) ? p1 : 0.f;
-                pp[e >> 1] = pack_bf16x2(p0, p1);
+                for (int e = 0; e < 64; e += 2) {
+                    const float2 t = ffma2(make_float2(__uint_as_float(xs[e]), __uint_as_float(xs[e + 1])), sl2x2,
+                                           nl2[e >> 1]);
+                    pp[e >> 1] = pack_bf16x2(ex2_approx(t.x), ex2_approx(t.y));
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 64; e += 2) {
+                    const float2 t = ffma2(make_float2(__uint_as_float(xs[e]), __uint_as_float(xs[e + 1])), sl2x2,
+                                           nl2[e >> 1]);
+                    float p0 = ex2_approx(t.x), p1 = ex2_approx(t.y);
+                    p0 = (a0 + e >= lo && a0 + e < p.L) ? p0 : 0.f;
+                    p1 = (a0 + e + 1 >= lo && a0 + e + 1 < p.L) ? p1 : 0.f;
+                    pp[e >> 1] = pack_bf16x2(p0, p1);
+                }
             }
             tmem_st32(tS + 32 * h, pp);
             tmem_wait_st();
@@ -432,11 +445,16 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dkdv_kernel(const __gri
             tmem_wait_ld();
             if (!(ok = meet()))
                 break;
+            const float2 *dl2 = reinterpret_cast<const float2 *>(dl);
+            const float2 zero2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int e = 0; e < 64; e += 2) {
                 const uint32_t pk = pp[e >> 1];
-                pd[e >> 1] = pack_bf16x2(bf16_lo(pk) * (__uint_as_float(xd[e]) - dl[e]),
-                                         bf16_hi(pk) * (__uint_as_float(xd[e + 1]) - dl[e + 1]));
+                const float2 nd = dl2[e >> 1];
+                const float2 t = fadd2(make_float2(__uint_as_float(xd[e]), __uint_as_float(xd[e + 1])),
+                                       make_float2(-nd.x, -nd.y));
+                const float2 ds = ffma2(make_float2(bf16_lo(pk), bf16_hi(pk)), t, zero2);
+                pd[e >> 1] = pack_bf16x2(ds.x, ds.y);
             }
             tmem_st32(tP + 32 * h, pd);
             tmem_wait_st();
@@ -646,6 +664,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dq_kernel(const __grid_
                 break;
             tc_fence_after();
             uint32_t pd[32];
+            const float2 sl2x2 = make_float2(sl2, sl2), nl2 = make_float2(nl, nl), ndl2 = make_float2(-dl, -dl);
+            const float2 zero2 = make_float2(0.f, 0.f);
+            const bool full = __all_sync(0xffffffffu, lim >= 64);  // no key of the half-tile masked
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 uint32_t xd[32];
@@ -654,12 +675,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dq_kernel(const __grid_
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                     const int x = 32 * c + e;
-                    float p0 = ex2_approx(fmaf(__uint_as_float(xs[x]), sl2, nl));
-                    float p1 = ex2_approx(fmaf(__uint_as_float(xs[x + 1]), sl2, nl));
-                    p0 = x < lim ? p0 : 0.f;
-                    p1 = x + 1 < lim ? p1 : 0.f;
-                    pd[x >> 1] = pack_bf16x2(p0 * (__uint_as_float(xd[e]) - dl),
-                                             p1 * (__uint_as_float(xd[e + 1]) - dl));
+                    const float2 t = ffma2(make_float2(__uint_as_float(xs[x]), __uint_as_float(xs[x + 1])), sl2x2, nl2);
+                    float2 pr = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+                    if (!full) {
+                        pr.x = x < lim ? pr.x : 0.f;
+                        pr.y = x + 1 < lim ? pr.y : 0.f;
+                    }
+                    const float2 g = fadd2(make_float2(__uint_as_float(xd[e]), __uint_as_float(xd[e + 1])), ndl2);
+                    const float2 ds = ffma2(pr, g, zero2);
+                    pd[x >> 1] = pack_bf16x2(ds.x, ds.y);
                 }
             }
             tmem_st32(tS + 32 * h, pd);
