@@ -1,6 +1,7 @@
 // SIMT kernels of the ring-attention library:
 //   * ra_attn_f32_kernel  exact fp32 ring-ordered attention (no tensor cores)
-//   * ra_permute_kernel   natural <-> striped token order, bit-exact copy
+//   * ra_permute_kernel   natural <-> striped token order, bit-exact copy (and a
+//                         32-bit-index variant with division by invariant integers)
 //   * ra_all_to_all_kernel sequence-sharded <-> head-sharded relayout (Ulysses)
 //   * ra_merge_kernel     running-softmax merge of one ring step's partials
 //   * ra_finalize_kernel  fp32 running result -> output dtype, natural order
@@ -135,6 +136,30 @@ void launch_fill_empty(float *out, float *lse, long long BH, int S, long long ro
     ra_fill_empty_kernel<<<grid, 256, 0, st>>>(out, lse, BH, S, row0, nrows, d);
 }
 
+// ---------------------------------------------------------------- index helpers
+// Division of n < 2^31 by an invariant d as a multiply-high and shift
+// (Granlund and Montgomery, "Division by Invariant Integers using
+// Multiplication", PLDI 1994, Theorem 4.2 with N = 31): with l = ceil(log2 d)
+// and m = ceil(2^(31 + l) / d), which fits in 32 bits, n / d = (n m) >> (31 + l).
+struct FastDiv {
+    uint32_t d, m, s;
+};
+
+FastDiv make_fastdiv(uint32_t d)
+{
+    uint32_t l = 0;
+    while ((1ull << l) < d)
+        ++l;
+    const uint32_t s = 31 + l;
+    const uint64_t m = ((1ull << s) + d - 1) / d;
+    return FastDiv{d, (uint32_t)m, s};
+}
+
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f)
+{
+    return (uint32_t)(((uint64_t)n * f.m) >> f.s);
+}
+
 // ---------------------------------------------------------------- permute
 // Striped row p = r L + a holds natural token t = a N + r.  Each thread moves
 // VEC-byte words; the grid walks destination rows, so writes are contiguous
@@ -173,6 +198,44 @@ __global__ void ra_permute_kernel(const VEC *__restrict__ src, VEC *__restrict__
     }
 }
 
+// The permutation with 32-bit index arithmetic (every word index < 2^31).
+template <typename VEC, int UNROLL>
+__global__ void ra_permute32_kernel(const VEC *__restrict__ src, VEC *__restrict__ dst, uint32_t n_words,
+                                    FastDiv wpr, FastDiv S, FastDiv L, FastDiv N, int inverse)
+{
+    const uint32_t stride = gridDim.x * blockDim.x;
+    for (uint32_t base = blockIdx.x * blockDim.x + threadIdx.x; base < n_words; base += stride * UNROLL) {
+        VEC v[UNROLL];
+        uint32_t at[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const uint32_t idx = base + u * stride;
+            at[u] = idx;
+            if (idx < n_words) {
+                const uint32_t row = fdiv(idx, wpr);
+                const uint32_t w = idx - row * wpr.d;
+                const uint32_t bh = fdiv(row, S);
+                const uint32_t x = row - bh * S.d;
+                // forward: x is the striped row p, read natural t(p)
+                // inverse: x is the natural token t, read striped p(t)
+                uint32_t other;
+                if (!inverse) {
+                    const uint32_t r = fdiv(x, L);
+                    other = (x - r * L.d) * N.d + r;
+                } else {
+                    const uint32_t a = fdiv(x, N);
+                    other = (x - a * N.d) * L.d + a;
+                }
+                v[u] = src[(size_t)(bh * S.d + other) * wpr.d + w];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u)
+            if (at[u] < n_words)
+                dst[at[u]] = v[u];
+    }
+}
+
 void launch_permute(const void *src, void *dst, long long rows_total, int S, int N,
                     long long row_bytes, int inverse, int sm_count, cudaStream_t st)
 {
@@ -183,6 +246,23 @@ void launch_permute(const void *src, void *dst, long long rows_total, int S, int
         const long long cap = (long long)sm_count * 8;
         return (int)(g < cap ? (g > 0 ? g : 1) : cap);
     };
+    const long long vec = row_bytes % 16 == 0 ? 16 : (row_bytes % 4 == 0 ? 4 : 1);
+    const long long words = rows_total * (row_bytes / vec);
+    // 32-bit path: every word index (and the grid-stride sum) below 2^31
+    if (words + 4ll * 8 * sm_count * threads < (1ll << 31)) {
+        const FastDiv fw = make_fastdiv((uint32_t)(row_bytes / vec)), fS = make_fastdiv((uint32_t)S),
+                      fL = make_fastdiv((uint32_t)L), fN = make_fastdiv((uint32_t)N);
+        if (vec == 16)
+            ra_permute32_kernel<uint4, 4><<<grid_for(words), threads, 0, st>>>(
+                (const uint4 *)src, (uint4 *)dst, (uint32_t)words, fw, fS, fL, fN, inverse);
+        else if (vec == 4)
+            ra_permute32_kernel<uint32_t, 4><<<grid_for(words), threads, 0, st>>>(
+                (const uint32_t *)src, (uint32_t *)dst, (uint32_t)words, fw, fS, fL, fN, inverse);
+        else
+            ra_permute32_kernel<uint8_t, 4><<<grid_for(words), threads, 0, st>>>(
+                (const uint8_t *)src, (uint8_t *)dst, (uint32_t)words, fw, fS, fL, fN, inverse);
+        return;
+    }
     if (row_bytes % 16 == 0) {
         const int wpr = (int)(row_bytes / 16);
         ra_permute_kernel<uint4, 4><<<grid_for(rows_total * wpr), threads, 0, st>>>(
@@ -257,6 +337,48 @@ __global__ void ra_all_to_all_kernel(const VEC *__restrict__ src, VEC *__restric
     }
 }
 
+// The relayout of ra_all_to_all_kernel with 32-bit index arithmetic and the
+// divisions above (every word index < 2^31).
+template <typename VEC, int UNROLL>
+__global__ void ra_all_to_all32_kernel(const VEC *__restrict__ src, VEC *__restrict__ dst, uint32_t n_words,
+                                       FastDiv wpr, FastDiv S, FastDiv Hg, FastDiv B, FastDiv L, FastDiv Hn,
+                                       int inverse)
+{
+    const uint32_t stride = gridDim.x * blockDim.x;
+    for (uint32_t base = blockIdx.x * blockDim.x + threadIdx.x; base < n_words; base += stride * UNROLL) {
+        VEC v[UNROLL];
+        uint32_t at[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const uint32_t idx = base + u * stride;
+            at[u] = idx;
+            if (idx < n_words) {
+                const uint32_t row = fdiv(idx, wpr);
+                const uint32_t w = idx - row * wpr.d;
+                uint32_t from;
+                if (!inverse) {
+                    const uint32_t r1 = fdiv(row, S), t = row - r1 * S.d;
+                    const uint32_t r2 = fdiv(r1, Hg), hl = r1 - r2 * Hg.d;
+                    const uint32_t g = fdiv(r2, B), b = r2 - g * B.d;
+                    const uint32_t i = fdiv(t, L), a = t - i * L.d;
+                    from = ((i * B.d + b) * Hn.d + g * Hg.d + hl) * L.d + a;
+                } else {
+                    const uint32_t r1 = fdiv(row, L), a = row - r1 * L.d;
+                    const uint32_t r2 = fdiv(r1, Hn), h = r1 - r2 * Hn.d;
+                    const uint32_t i = fdiv(r2, B), b = r2 - i * B.d;
+                    const uint32_t g = fdiv(h, Hg), hl = h - g * Hg.d;
+                    from = ((g * B.d + b) * Hg.d + hl) * S.d + i * L.d + a;
+                }
+                v[u] = src[(size_t)from * wpr.d + w];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u)
+            if (at[u] < n_words)
+                dst[at[u]] = v[u];
+    }
+}
+
 void launch_all_to_all(const void *src, void *dst, int B, int Hn, int S, int n_dev, long long row_bytes,
                        int inverse, int sm_count, cudaStream_t st)
 {
@@ -268,6 +390,24 @@ void launch_all_to_all(const void *src, void *dst, int B, int Hn, int S, int n_d
         const long long cap = (long long)sm_count * 8;
         return (int)(g < cap ? (g > 0 ? g : 1) : cap);
     };
+    const long long vec = row_bytes % 16 == 0 ? 16 : (row_bytes % 4 == 0 ? 4 : 1);
+    const long long words = rows_total * (row_bytes / vec);
+    // 32-bit path: every word index (and the grid-stride sum) below 2^31
+    if (words + 4ll * 8 * sm_count * threads < (1ll << 31)) {
+        const FastDiv fw = make_fastdiv((uint32_t)(row_bytes / vec)), fS = make_fastdiv((uint32_t)S),
+                      fHg = make_fastdiv((uint32_t)Hg), fB = make_fastdiv((uint32_t)B),
+                      fL = make_fastdiv((uint32_t)L), fHn = make_fastdiv((uint32_t)Hn);
+        if (vec == 16)
+            ra_all_to_all32_kernel<uint4, 4><<<grid_for(words), threads, 0, st>>>(
+                (const uint4 *)src, (uint4 *)dst, (uint32_t)words, fw, fS, fHg, fB, fL, fHn, inverse);
+        else if (vec == 4)
+            ra_all_to_all32_kernel<uint32_t, 4><<<grid_for(words), threads, 0, st>>>(
+                (const uint32_t *)src, (uint32_t *)dst, (uint32_t)words, fw, fS, fHg, fB, fL, fHn, inverse);
+        else
+            ra_all_to_all32_kernel<uint8_t, 4><<<grid_for(words), threads, 0, st>>>(
+                (const uint8_t *)src, (uint8_t *)dst, (uint32_t)words, fw, fS, fHg, fB, fL, fHn, inverse);
+        return;
+    }
     if (row_bytes % 16 == 0) {
         const int wpr = (int)(row_bytes / 16);
         ra_all_to_all_kernel<uint4, 4><<<grid_for(rows_total * wpr), threads, 0, st>>>(
