@@ -88,22 +88,27 @@ def attention_backward(q, k, v, dout, causal: bool = False,
 
 def dq_rows(q, k, v, dout, rows, causal: bool = False) -> np.ndarray:
     """dq for selected flattened (b, h, t) rows only: each row needs its own
-    softmax row, dO row and the keys and values, O(S d) per row."""
-    qa, ka, va, da = (_f64(t) for t in (q, k, v, dout))
-    B, H, S, d = qa.shape
-    grp = H // ka.shape[1]
+    softmax row, dO row and the keys and values, O(S d) per row.  Only the
+    kv heads the rows use are widened to fp64."""
+    B, H, S, d = q.shape
+    grp = H // k.shape[1]
     c = 1.0 / np.sqrt(d)
     rows = np.asarray(rows, dtype=np.int64).ravel()
     out = np.empty((rows.size, d))
+    heads = {}
     for n, r in enumerate(rows):
         b, h, t = int(r // (H * S)), int(r // S % H), int(r % S)
         g = h // grp
-        kk = ka[b, g, :t + 1] if causal else ka[b, g]
-        vv = va[b, g, :t + 1] if causal else va[b, g]
-        s = (kk @ qa[b, h, t]) * c
+        if (b, g) not in heads:
+            heads[(b, g)] = (_f64(k[b, g]), _f64(v[b, g]))
+        kg, vg = heads[(b, g)]
+        kk = kg[:t + 1] if causal else kg
+        vv = vg[:t + 1] if causal else vg
+        qt, dt = _f64(q[b, h, t]), _f64(dout[b, h, t])
+        s = (kk @ qt) * c
         p = np.exp(s - s.max())
         p /= p.sum()
-        dp = vv @ da[b, h, t]
+        dp = vv @ dt
         ds = p * (dp - (p * dp).sum())
         out[n] = c * (ds @ kk)
     return out

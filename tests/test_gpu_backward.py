@@ -91,18 +91,23 @@ def test_backward_deterministic():
         assert torch.equal(x, y)
 
 
-def test_backward_workload_32k_properties_and_sampled_rows():
-    """32K tokens, 32 query heads over 8 kv heads, causal, N = 4 (the 32K
-    workload's shape): dq on sampled rows against the oracle row by row, and
-    over all keys the identities sum_u dV = sum_t dO (per kv head) and
-    sum_u dK = 0, which the whole dK and dV must satisfy."""
-    w = inputs.WORKLOADS["ring4-s32k-h32kv8-d128-causal-contiguous"]
+@pytest.mark.parametrize("name", ["ring4-s32k-h32kv8-d128-causal-contiguous",
+                                  "ring8-s256k-h32kv8-d128-causal-striped"])
+def test_backward_workload_properties_and_sampled_rows(name):
+    """A workload's full shape (32K tokens over 4 blocks; 256K tokens over 8,
+    striped, as the bench's backward measurement runs): dq on sampled rows
+    against the oracle row by row, and over all keys the identities
+    sum_u dV = sum_t dO (per kv head) and sum_u dK = 0, which the whole dK and
+    dV must satisfy."""
+    w = inputs.WORKLOADS[name]
+    layout = "striped"
     q, k, v = inputs.workload_qkv(w, device="cuda")
-    dout = _dout(w.B, w.H, w.S, w.d, seed=77).cuda()
-    out, lse = ra.forward(q, k, v, n_blocks=w.n_blocks, layout="striped", causal=True)
-    dq, dk, dv = ra.backward(q, k, v, out, lse, dout, w.n_blocks, layout="striped", causal=True)
+    g = torch.Generator(device="cuda").manual_seed(77)
+    dout = torch.randn(q.shape, generator=g, device="cuda").to(torch.bfloat16)
+    out, lse = ra.forward(q, k, v, n_blocks=w.n_blocks, layout=layout, causal=True)
+    dq, dk, dv = ra.backward(q, k, v, out, lse, dout, w.n_blocks, layout=layout, causal=True)
     ra.check()
-    rows = inputs.sample_rows(w.B, w.H, w.S, w.n_blocks, n=96, seed=7)
+    rows = inputs.sample_rows(w.B, w.H, w.S, w.n_blocks, n=48 if w.S > 65536 else 96, seed=7)
     ref = dq_rows(q.cpu(), k.cpu(), v.cpu(), dout.cpu(), rows, causal=True)
     got = dq.float().cpu().double().numpy().reshape(-1, w.d)[rows]
     assert np.abs(got - ref).max() <= REL_MAX * np.abs(ref).max()
