@@ -76,6 +76,8 @@ def _load():
             ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
             ctypes.c_int]
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_set_threads.argtypes = [ctypes.c_int]
+        lib.oracle_set_threads.restype = None
         _lib = lib
     return _lib
 
@@ -83,6 +85,11 @@ def _load():
 def num_threads() -> int:
     """OpenMP threads the oracle runs on (OMP_NUM_THREADS or all cores)."""
     return int(_load().oracle_num_threads())
+
+
+def set_threads(n: int) -> None:
+    """Run the oracle on n threads from now on (0: all cores)."""
+    _load().oracle_set_threads(int(n))
 
 
 def _as_host_array(x) -> Tuple[np.ndarray, int]:

@@ -186,3 +186,14 @@ int oracle_num_threads(void)
     }
     return n;
 }
+
+/* Thread count for the oracle's parallel loops from now on (0 restores all
+ * cores); the benchmark reports a one-core rate beside the all-core one. */
+void oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    omp_set_num_threads(n > 0 ? n : omp_get_num_procs());
+#else
+    (void)n;
+#endif
+}
