@@ -19,7 +19,9 @@
 //     128-byte swizzled 64-column slabs), warp 1 issues tcgen05.mma,
 //     warps 4-7 and 8-11 run the online softmax for query tile 0 and 1;
 //   * S = Q K^T goes to TMEM (fp32, 128 lanes x 128 columns per tile); each
-//     softmax thread reads its row once (two 64-column loads, one wait),
+//     softmax thread reads its row once (two 64-column loads, one wait; the
+//     loads of an unmasked tile also reduce the row to its max, a Blackwell
+//     Ultra form of tcgen05.ld),
 //     writes P = exp2(S log2e/sqrt(d) - m) back over the same columns as
 //     packed bf16, and O += P V reads P from TMEM as the A operand and V from
 //     shared memory (MN-major);
@@ -159,7 +161,9 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap *tm, i
 
 // One online-softmax step for the query row this thread owns.  The row's 128
 // scores of the current key tile are read from TMEM once (two 64-column
-// loads, one wait); columns at or past `lim` count as -inf when MASK.  The
+// loads, one wait); on unmasked tiles the loads also return each half row's
+// maximum (tcgen05.ld.red), so no max pass over the registers is needed;
+// columns at or past `lim` count as -inf when MASK.  The
 // running max m (log2 domain, scores scaled by sl2 = log2e / sqrt(d)) only
 // moves when the tile max exceeds it by more than 2^8, and then O (in TMEM,
 // when has_o) and l are rescaled by 2^(m_old - m_new); the final division
@@ -173,20 +177,26 @@ __device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, int lim, 
     const uint32_t ninf = __float_as_uint(-INFINITY);
     float ma = -INFINITY, mb = -INFINITY;
     uint32_t xa[64], xb[64];
-    tmem_ld64(tS, xa);
-    tmem_ld64(tS + 64, xb);
-    tmem_wait_ld();
     if (MASK) {
+        tmem_ld64(tS, xa);
+        tmem_ld64(tS + 64, xb);
+        tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 64; ++e) {
             xa[e] = e < lim ? xa[e] : ninf;
             xb[e] = e + 64 < lim ? xb[e] : ninf;
         }
-    }
 #pragma unroll
-    for (int e = 0; e < 64; e += 2) {
-        ma = max3f(ma, __uint_as_float(xa[e]), __uint_as_float(xa[e + 1]));
-        mb = max3f(mb, __uint_as_float(xb[e]), __uint_as_float(xb[e + 1]));
+        for (int e = 0; e < 64; e += 2) {
+            ma = max3f(ma, __uint_as_float(xa[e]), __uint_as_float(xa[e + 1]));
+            mb = max3f(mb, __uint_as_float(xb[e]), __uint_as_float(xb[e + 1]));
+        }
+    } else {
+        // the tensor-memory load reduces each half row to its maximum itself
+        tmem_ld64_max(tS, xa, ma);
+        tmem_ld64_max(tS + 64, xb, mb);
+        tmem_wait_ld();
+        asm volatile("" : "+f"(ma), "+f"(mb));  // keep every use of the maxima after the wait
     }
     const float m_tile = fmaxf(ma, mb) * sl2;  // -inf stays -inf
     const bool resc = m_tile > m_run + LAZY_RESCALE_LOG2;

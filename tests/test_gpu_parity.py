@@ -145,6 +145,20 @@ def test_bf16_large_scores_stress_running_max():
     ra.check()
 
 
+def test_bf16_huge_scores_need_the_true_row_max():
+    """Scores spanning about +-600 in the log2 domain: 2^(s - m) stays
+    finite only if m is at least the tile's true row maximum, so a row max
+    taken from the wrong columns or rows overflows to inf / NaN here (the
+    unmasked tiles take it from the tensor-memory load's own reduction)."""
+    q, k, v = inputs.make_qkv(1, 2, 1, 1024, 128, seed=12, spike_frac=0.05, spike_scale=16.0)
+    q, k, v = _dev(q * 6, k, v)
+    for layout in ("contiguous", "striped"):
+        out, lse = ra.forward(q, k, v, n_blocks=4, layout=layout, causal=True)
+        assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+        _check(out, lse, q, k, v, True)
+    ra.check()
+
+
 # ---------------------------------------------------------------- named workloads
 
 def _workload(name):
