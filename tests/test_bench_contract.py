@@ -28,3 +28,33 @@ def test_reference_arm_prints_one_contract_line():
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["value"] > 0
+
+
+@pytest.mark.gpu
+def test_gpu_arm_prints_one_contract_line():
+    """The GPU arm on the 32K workload: one line with the contract's keys, the
+    roofline and end-to-end objects, and an end-to-end figure that moves the
+    step's inputs and outputs through host memory."""
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "2", "--warmup", "3",
+                          "--workload", "ring4-s32k-h32kv8-d128-causal-contiguous", "--no-cpu-baseline",
+                          "--no-backward"],
+                         capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "dtype", "data", "config", "roofline", "e2e", "clocks", "gpu_launches"):
+        assert key in d, key
+    assert d["n_gpus"] == 1 and d["steps"] == 2 and d["warmup"] == 3 and d["value"] > 0
+    r = d["roofline"]
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and 0 < r["frac"] == pytest.approx(r["achieved"] / r["peak"])
+    e = d["e2e"]
+    # q, k, v in (bf16) and out (bf16) + lse (fp32) back, every step
+    S, H, Hkv, dh = 32768, 32, 8, 128
+    assert e["h2d_bytes_per_step"] == 2 * S * dh * (H + 2 * Hkv)
+    assert e["d2h_bytes_per_step"] == 2 * S * dh * H + 4 * S * H
+    assert 0 < e["value"] and e["ms_per_step"] > 0 and e["serial_ms_per_step"] > 0
+    # the copies are inside the timed region: the end-to-end step cannot beat the device-resident one
+    assert e["ms_per_step"] >= 0.98 * d["ms_per_step"]
+    assert d["gpu_launches"] >= d["steps"]
