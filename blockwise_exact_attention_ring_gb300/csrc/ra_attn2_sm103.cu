@@ -17,8 +17,9 @@
 //     buffers: S(j + 1) and S(j + 2) are computed while the softmax of S(j)
 //     runs, and only P(j) -> O += P V waits for the softmax;
 //   * eight softmax warps per CTA, two per TMEM lane quarter: each thread
-//     owns half a row (64 scores), the two halves exchange their row max
-//     through shared memory each step;
+//     owns half a row (64 scores) whose max comes with its tensor-memory
+//     load (tcgen05.ld.red, except on masked tiles), and the two halves
+//     exchange their row max through shared memory each step;
 //   * the leader CTA (rank 0) issues all MMAs; its barriers receive the
 //     peer's TMA bytes and softmax arrivals; MMA completions are multicast to
 //     both CTAs;
@@ -394,22 +395,25 @@ ra_attn_pair_kernel(const __grid_constant__ PairParams p)
                 tc_fence_after();
                 uint32_t x[64];
                 const uint32_t tS = tbase + buf * 128;
-                tmem_ld64(tS + h * 64, x);
+                float mine;
+                tmem_ld64_max(tS + h * 64, x, mine);  // the load also reduces the half row to its max
                 tmem_wait_ld();
+                asm volatile("" : "+f"(mine));  // keep every use of the max after the wait
                 const int lim = ra_key_limit(w.cls, a, p.L) - w.tb * RA_TILE - h * 64;
                 if (!__all_sync(0xffffffffu, lim >= 64)) {
+                    // masked tile: the max must skip the hidden columns
                     const uint32_t ninf = __float_as_uint(-INFINITY);
 #pragma unroll
                     for (int e = 0; e < 64; ++e)
                         x[e] = e < lim ? x[e] : ninf;
-                }
-                float ma = -INFINITY, mb = -INFINITY;
+                    float ma = -INFINITY, mb = -INFINITY;
 #pragma unroll
-                for (int e = 0; e < 64; e += 4) {
-                    ma = max3f(ma, __uint_as_float(x[e]), __uint_as_float(x[e + 1]));
-                    mb = max3f(mb, __uint_as_float(x[e + 2]), __uint_as_float(x[e + 3]));
+                    for (int e = 0; e < 64; e += 4) {
+                        ma = max3f(ma, __uint_as_float(x[e]), __uint_as_float(x[e + 1]));
+                        mb = max3f(mb, __uint_as_float(x[e + 2]), __uint_as_float(x[e + 3]));
+                    }
+                    mine = fmaxf(ma, mb);
                 }
-                const float mine = fmaxf(ma, mb);
                 float theirs;
                 if (!(ok = exchange(gstep & 1, (gstep >> 1) & 1, mine, theirs)))
                     break;
