@@ -12,6 +12,10 @@
 // written for Blackwell:
 //
 //   * one persistent CTA per SM (512 TMEM columns, ~193 KB shared memory);
+//     where every kv head serves four or more query heads, the CTAs run as
+//     clusters of two whose units walk the same key/value tiles (the two
+//     head pairs of a group), and each K and V tile is loaded once for both
+//     by TMA multicast (CTA 0 issues K, CTA 1 issues V);
 //   * a unit of work is a PAIR of 128-row query tiles that share a kv head
 //     (two heads of one grouped-query group, or two adjacent tiles of one
 //     head), so every key/value tile staged in shared memory feeds two tiles;
@@ -41,7 +45,7 @@
 #include <cudaTypedefs.h>
 
 #include "ra_internal.h"
-#include "ra_ptx.cuh"
+#include "ra_ptx_pair.cuh"
 
 namespace ra {
 
@@ -143,6 +147,14 @@ __device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, volatile in
     return mbar_wait(bar, parity, abort, timeout, &g_ra_status, site);
 }
 
+// Waits on barriers that the peer CTA of a cluster also feeds (multicast
+// copies and MMA-completion arrivals): cluster-scope acquire.
+__device__ __forceinline__ bool wait1c(uint32_t bar, uint32_t parity, volatile int *abort,
+                                       uint64_t timeout, unsigned int site)
+{
+    return mbar_wait_cluster(bar, parity, abort, timeout, &g_ra_status, site);
+}
+
 // Wait that ignores the abort flag: used to drain work already in flight.
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout)
 {
@@ -157,6 +169,16 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap *tm, i
 #pragma unroll
     for (int h = 0; h < D / 64; ++h)
         tma_load_2d(dst + h * Cfg<D>::SLAB, tm, h * 64, row, bar, pol);
+}
+
+// The same tile into both CTAs of a cluster (same offsets, same barrier).
+template <int D>
+__device__ __forceinline__ void load_tile_both(uint32_t dst, const CUtensorMap *tm, int row, uint32_t bar,
+                                               uint64_t pol)
+{
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h)
+        tma_load_2d_mc(dst + h * Cfg<D>::SLAB, tm, h * 64, row, bar, (uint16_t)3, pol);
 }
 
 // One online-softmax step for the query row this thread owns.  The row's 128
@@ -242,7 +264,13 @@ __device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, int lim, 
     }
 }
 
-template <int D>
+// CL = 1: one CTA per SM.  CL = 2: clusters of two CTAs whose units have the
+// same kv head, rank and query tile slot (the two head pairs of a group of
+// four or more query heads), so both walk the same key/value tiles: CTA 0
+// loads each K tile and CTA 1 each V tile into BOTH CTAs' shared memory by
+// TMA multicast, and a stage is reloaded only after both CTAs' MMAs have
+// consumed it (each MMA warp commits to the empty barrier of both CTAs).
+template <int D, int CL>
 __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid_constant__ TcParams p)
 {
     using C = Cfg<D>;
@@ -261,11 +289,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
         mbar_init(bar(ctrl->q_empty), 1);
         for (int s = 0; s < C::KSTAGES; ++s) {
             mbar_init(bar(ctrl->k_full[s]), 1);
-            mbar_init(bar(ctrl->k_empty[s]), 1);
+            mbar_init(bar(ctrl->k_empty[s]), CL);
         }
         for (int s = 0; s < C::VSTAGES; ++s) {
             mbar_init(bar(ctrl->v_full[s]), 1);
-            mbar_init(bar(ctrl->v_empty[s]), 1);
+            mbar_init(bar(ctrl->v_empty[s]), CL);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(ctrl->s_full[t]), 1);
@@ -289,11 +317,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
     }
     tc_fence_before();
     __syncthreads();
+    if (CL == 2)
+        cluster_sync_all();  // the peer's barriers exist before any multicast reaches them
     tc_fence_after();
     const uint32_t tmem = ctrl->tmem_base;
     volatile int *abort = &ctrl->abort;
     const uint64_t tmo = p.timeout_ns;
     const int group = p.H / p.Hkv;
+    const int crank = CL == 2 ? (int)cluster_ctarank() : 0;
+    // unit of round r: clusters are dealt unit pairs (2m, 2m + 1) in snake order
+    auto unit_of = [&](int r) { return CL * unit_index(r, blockIdx.x / CL, gridDim.x / CL) + crank; };
+    auto kv_wait = [&](uint32_t b, uint32_t parity, unsigned int site) {
+        return CL == 2 ? wait1c(b, parity, abort, tmo, site) : wait1(b, parity, abort, tmo, site);
+    };
+    auto kv_release = [&](uint32_t b) {
+        if (CL == 2)
+            mma_commit_mc(b, (uint16_t)3);
+        else
+            mma_commit(b);
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -303,7 +345,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
             uint32_t kcnt = 0, vcnt = 0, qcnt = 0;
             bool ok = true;
             for (int r = 0; ok; ++r) {
-                const int u = unit_index(r, blockIdx.x, gridDim.x);
+                const int u = unit_of(r);
                 if (u >= p.n_units)
                     break;
                 const RaUnit U = ra_unit_decode(p.sp, u);
@@ -323,18 +365,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
                 for (; w.valid(); w.advance()) {
                     const int row = kvbh * p.S + w.j * p.L + w.tb * RA_TILE;
                     const int ks = kcnt % C::KSTAGES;
-                    if (!(ok = wait1(bar(ctrl->k_empty[ks]), ((kcnt / C::KSTAGES) & 1) ^ 1,
-                                         abort, tmo, SITE_K_EMPTY)))
+                    if (!(ok = kv_wait(bar(ctrl->k_empty[ks]), ((kcnt / C::KSTAGES) & 1) ^ 1,
+                                       SITE_K_EMPTY)))
                         break;
                     mbar_arrive_expect_tx(bar(ctrl->k_full[ks]), C::TILE);
-                    load_tile<D>(sK + ks * C::TILE, &p.tm_k, row, bar(ctrl->k_full[ks]), pol_kv);
+                    if (CL == 1)
+                        load_tile<D>(sK + ks * C::TILE, &p.tm_k, row, bar(ctrl->k_full[ks]), pol_kv);
+                    else if (crank == 0)
+                        load_tile_both<D>(sK + ks * C::TILE, &p.tm_k, row, bar(ctrl->k_full[ks]), pol_kv);
                     ++kcnt;
                     const int vs = vcnt % C::VSTAGES;
-                    if (!(ok = wait1(bar(ctrl->v_empty[vs]), ((vcnt / C::VSTAGES) & 1) ^ 1,
-                                         abort, tmo, SITE_V_EMPTY)))
+                    if (!(ok = kv_wait(bar(ctrl->v_empty[vs]), ((vcnt / C::VSTAGES) & 1) ^ 1,
+                                       SITE_V_EMPTY)))
                         break;
                     mbar_arrive_expect_tx(bar(ctrl->v_full[vs]), C::TILE);
-                    load_tile<D>(sV + vs * C::TILE, &p.tm_v, row, bar(ctrl->v_full[vs]), pol_kv);
+                    if (CL == 1)
+                        load_tile<D>(sV + vs * C::TILE, &p.tm_v, row, bar(ctrl->v_full[vs]), pol_kv);
+                    else if (crank == 1)
+                        load_tile_both<D>(sV + vs * C::TILE, &p.tm_v, row, bar(ctrl->v_full[vs]), pol_kv);
                     ++vcnt;
                 }
             }
@@ -379,30 +427,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
             uint32_t kcnt = 0, vcnt = 0, qcnt = 0, pcnt = 0;
             bool ok = true;
             for (int r = 0; ok; ++r) {
-                const int u = unit_index(r, blockIdx.x, gridDim.x);
+                const int u = unit_of(r);
                 if (u >= p.n_units)
                     break;
                 const int n = ra_unit_decode(p.sp, u).cost;
                 if (!(ok = wait1(bar(ctrl->q_full), qcnt & 1, abort, tmo, SITE_Q_FULL)))
                     break;
                 int ks = kcnt % C::KSTAGES;
-                if (!(ok = wait1(bar(ctrl->k_full[ks]), (kcnt / C::KSTAGES) & 1, abort, tmo,
-                                     SITE_K_FULL)))
+                if (!(ok = kv_wait(bar(ctrl->k_full[ks]), (kcnt / C::KSTAGES) & 1, SITE_K_FULL)))
                     break;
                 tc_fence_after();
                 issue_s(0, ks);
                 mma_commit(bar(ctrl->s_full[0]));
                 issue_s(1, ks);
                 mma_commit(bar(ctrl->s_full[1]));
-                mma_commit(bar(ctrl->k_empty[ks]));
+                kv_release(bar(ctrl->k_empty[ks]));
                 ++kcnt;
                 if (n == 1)
                     mma_commit(bar(ctrl->q_empty));
                 for (int jj = 0; jj < n; ++jj) {
                     const int vs = vcnt % C::VSTAGES;
                     const bool more = jj + 1 < n;
-                    if (!(ok = wait1(bar(ctrl->v_full[vs]), (vcnt / C::VSTAGES) & 1, abort, tmo,
-                                         SITE_V_FULL)))
+                    if (!(ok = kv_wait(bar(ctrl->v_full[vs]), (vcnt / C::VSTAGES) & 1, SITE_V_FULL)))
                         break;
                     if (jj == 0 && qcnt > 0 &&
                         !(ok = wait1(bar(ctrl->o_free[0]), (qcnt - 1) & 1, abort, tmo, SITE_O_FREE)))
@@ -414,8 +460,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
                     mma_commit(bar(ctrl->o_done[0]));
                     if (more) {
                         ks = kcnt % C::KSTAGES;
-                        if (!(ok = wait1(bar(ctrl->k_full[ks]), (kcnt / C::KSTAGES) & 1, abort,
-                                             tmo, SITE_K_FULL)))
+                        if (!(ok = kv_wait(bar(ctrl->k_full[ks]), (kcnt / C::KSTAGES) & 1, SITE_K_FULL)))
                             break;
                         tc_fence_after();
                         issue_s(0, ks);
@@ -429,12 +474,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
                     tc_fence_after();
                     issue_pv(1, vs, jj > 0);
                     mma_commit(bar(ctrl->o_done[1]));
-                    mma_commit(bar(ctrl->v_empty[vs]));
+                    kv_release(bar(ctrl->v_empty[vs]));
                     ++vcnt;
                     if (more) {
                         issue_s(1, ks);
                         mma_commit(bar(ctrl->s_full[1]));
-                        mma_commit(bar(ctrl->k_empty[ks]));
+                        kv_release(bar(ctrl->k_empty[ks]));
                         ++kcnt;
                         if (jj + 2 == n)
                             mma_commit(bar(ctrl->q_empty));
@@ -459,7 +504,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
         uint32_t scnt = 0, ocnt = 0;
         bool ok = true;
         for (int rr = 0; ok; ++rr) {
-            const int u = unit_index(rr, blockIdx.x, gridDim.x);
+            const int u = unit_of(rr);
             if (u >= p.n_units)
                 break;
             const RaUnit U = ra_unit_decode(p.sp, u);
@@ -542,6 +587,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
+    if (CL == 2)
+        cluster_sync_all();  // no CTA leaves while the peer may still signal or fill it
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -578,18 +625,54 @@ bool encode_rows(CUtensorMap *tm, const void *base, long long rows, int d)
     return r == CUDA_SUCCESS;
 }
 
+template <int D, int CL>
+cudaError_t set_smem_attr()
+{
+    static bool done = false;
+    if (!done) {
+        cudaError_t e = cudaFuncSetAttribute(ra_attn_tc_kernel<D, CL>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
+        if (e != cudaSuccess)
+            return e;
+        done = true;
+    }
+    return cudaSuccess;
+}
+
+// Clusters of two that can be resident at once (one CTA per SM), queried once.
+template <int D>
+int max_pair_clusters()
+{
+    static int n = -1;
+    if (n < 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2);
+        cfg.blockDim = dim3(NUM_THREADS);
+        cfg.dynamicSmemBytes = Cfg<D>::SMEM;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = 2;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        int c = 0;
+        if (cudaOccupancyMaxActiveClusters(&c, ra_attn_tc_kernel<D, 2>, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            c = 0;
+        }
+        n = c;
+    }
+    return n;
+}
+
 template <int D>
 cudaError_t launch_d(const TcLaunch &a, cudaStream_t st)
 {
     using C = Cfg<D>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(ra_attn_tc_kernel<D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess)
-            return e;
-        attr_set = true;
-    }
+    cudaError_t e = set_smem_attr<D, 1>();
+    if (e != cudaSuccess)
+        return e;
     TcParams p;
     memset(&p, 0, sizeof(p));
     if (!encode_rows(&p.tm_q, a.q, (long long)a.B * a.H * a.S, D) ||
@@ -612,8 +695,35 @@ cudaError_t launch_d(const TcLaunch &a, cudaStream_t st)
     p.timeout_ns = a.timeout_ns;
     if (p.n_units <= 0)
         return cudaSuccess;
+    // Clusters need units (2m, 2m + 1) with one key/value walk: two head
+    // pairs of one kv head next to each other in the order, i.e. an even
+    // number of head pairs per kv head.
+    const int pairs_per_kv = p.sp.head_pairs ? (a.H / a.Hkv) / 2 : 0;
+    if (a.cluster == 2 && pairs_per_kv >= 2 && pairs_per_kv % 2 == 0 && p.n_units % 2 == 0) {
+        if ((e = set_smem_attr<D, 2>()) != cudaSuccess)
+            return e;
+        const int max_cl = max_pair_clusters<D>();
+        if (max_cl >= 1) {
+            const int pairs = p.n_units / 2;
+            const int clusters = pairs < max_cl ? pairs : max_cl;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2 * clusters);
+            cfg.blockDim = dim3(NUM_THREADS);
+            cfg.dynamicSmemBytes = C::SMEM;
+            cfg.stream = st;
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = 2;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            e = cudaLaunchKernelEx(&cfg, ra_attn_tc_kernel<D, 2>, p);
+            return e != cudaSuccess ? e : cudaGetLastError();
+        }
+    }
     const int grid = p.n_units < a.sm_count ? p.n_units : a.sm_count;
-    ra_attn_tc_kernel<D><<<grid, NUM_THREADS, C::SMEM, st>>>(p);
+    ra_attn_tc_kernel<D, 1><<<grid, NUM_THREADS, C::SMEM, st>>>(p);
     return cudaGetLastError();
 }
 

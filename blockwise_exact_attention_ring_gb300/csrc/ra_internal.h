@@ -49,6 +49,7 @@ struct TcLaunch {
     int out_f32;
     unsigned long long timeout_ns;
     int sm_count;
+    int cluster;                 // 2: share K/V loads between CTA pairs where the units allow
 };
 
 // Backward pass (bf16, d in {64, 128}): delta = rowsum(dout * out), then the

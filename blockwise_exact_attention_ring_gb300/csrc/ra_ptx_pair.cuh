@@ -1,6 +1,8 @@
-// Inline-PTX helpers for kernels launched as clusters of two CTAs that run
-// tcgen05 with cta_group::2: one MMA spans both CTAs' tensor memory and
-// shared memory.  Builds on the single-CTA helpers of ra_ptx.cuh.
+// Inline-PTX helpers for kernels launched as clusters of two CTAs: the
+// CTA-pair kernel, whose tcgen05 MMAs use cta_group::2 (one MMA spans both
+// CTAs' tensor memory and shared memory), and the single-CTA kernel's
+// cluster form, whose two CTAs share each key/value tile load by TMA
+// multicast.  Builds on the single-CTA helpers of ra_ptx.cuh.
 #pragma once
 
 #include "ra_ptx.cuh"
@@ -73,6 +75,28 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *tmap,
         ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;"
         ::"r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar_cluster), "l"(policy)
         : "memory");
+}
+
+// 2-D tiled TMA load multicast to the CTAs in `mask`: the box lands at the
+// same shared-memory offset `dst` in each of them and completes `bar` (same
+// offset) in each.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void *tmap, int x, int y, uint32_t bar,
+                                               uint16_t mask, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;"
+        ::"r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar), "h"(mask), "l"(policy)
+        : "memory");
+}
+
+// Arrive once on the mbarrier at offset `bar` in each CTA of `mask` when
+// every tcgen05 operation this thread issued so far (cta_group::1) has
+// completed.
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+                 " [%0], %1;" ::"r"(bar), "h"(mask) : "memory");
 }
 
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols)

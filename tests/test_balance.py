@@ -130,3 +130,22 @@ def test_backward_kernels_cover_every_visible_tile_pair_once(B, H, Hkv, S, N, la
                 assert len(set(rows[:, 4].tolist())) == 1 and len(set(rows[:, 5].tolist())) == 1
             else:
                 assert len(set(rows[:, 1].tolist())) == 1 and len(set(rows[:, 3].tolist())) == 1
+
+
+@pytest.mark.parametrize("B,H,Hkv,S,N", [(1, 8, 2, 1024, 4), (2, 16, 4, 768, 3), (1, 32, 8, 262144, 8),
+                                         (1, 8, 1, 640, 5), (1, 32, 8, 1048576, 32)])
+@pytest.mark.parametrize("layout,causal", [("contiguous", True), ("striped", True), ("striped", False)])
+def test_cluster_pairs_share_one_key_walk(B, H, Hkv, S, N, layout, causal):
+    """Kernel variant 3 deals units (2m, 2m + 1) to the two CTAs of a cluster,
+    which share every key/value tile load: with four or more query heads per
+    kv head (an even number of head pairs), both units of each pair have the
+    same kv head, rank and query tiles, so they walk the same key tiles, and
+    they differ in their query heads."""
+    u = ra.schedule_units(B, H, Hkv, S, N, layout, causal)
+    assert len(u) % 2 == 0
+    a, b = u[0::2], u[1::2]
+    grp = H // Hkv
+    kv = lambda bh: (bh // H) * Hkv + (bh % H) // grp
+    assert np.array_equal(kv(a[:, 0]), kv(b[:, 0]))
+    assert np.array_equal(a[:, [1, 3, 4, 5, 6]], b[:, [1, 3, 4, 5, 6]])
+    assert np.all(a[:, 0] != b[:, 0]) and np.all(a[:, 2] != b[:, 2])
