@@ -49,8 +49,11 @@ def test_short_wait_limit_does_not_trip_a_healthy_run():
     L = ra.lib()
     L.ra_set_wait_timeout_ns(100_000_000)
     try:
-        q, k, v = (t.cuda() for t in inputs.make_qkv(1, 4, 2, 4096, 128, seed=78))
-        ra.forward(q, k, v, n_blocks=4, causal=True)
-        ra.check()
+        # group 2 runs one CTA per unit; group 4 runs CTA pairs whose waits
+        # include the peer's multicast copies and stage releases
+        for H, Hkv in ((4, 2), (8, 2)):
+            q, k, v = (t.cuda() for t in inputs.make_qkv(1, H, Hkv, 4096, 128, seed=78))
+            ra.forward(q, k, v, n_blocks=4, causal=True)
+            ra.check()
     finally:
         L.ra_set_wait_timeout_ns(0)
