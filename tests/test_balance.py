@@ -149,3 +149,22 @@ def test_cluster_pairs_share_one_key_walk(B, H, Hkv, S, N, layout, causal):
     assert np.array_equal(kv(a[:, 0]), kv(b[:, 0]))
     assert np.array_equal(a[:, [1, 3, 4, 5, 6]], b[:, [1, 3, 4, 5, 6]])
     assert np.all(a[:, 0] != b[:, 0]) and np.all(a[:, 2] != b[:, 2])
+
+
+@pytest.mark.parametrize("layout,causal", [("contiguous", True), ("striped", True), ("contiguous", False)])
+def test_cluster_pairs_within_one_devices_step(layout, causal):
+    """ra_forward_block restricts the unit space to one rank and one ring
+    step; its units still pair up (2m, 2m + 1) on one key walk, so the
+    K/V-sharing CTA pairs serve one device's step as well."""
+    B, H, Hkv, S, N = 1, 8, 2, 2048, 4
+    grp = H // Hkv
+    kv = lambda bh: (bh // H) * Hkv + (bh % H) // grp
+    for i in range(N):
+        for s in range(N):
+            u = ra.block_units(B, H, Hkv, S, N, layout, causal, i, s)
+            assert len(u) % 2 == 0
+            if len(u) == 0:
+                continue
+            a, b = u[0::2], u[1::2]
+            assert np.array_equal(kv(a[:, 0]), kv(b[:, 0]))
+            assert np.array_equal(a[:, [1, 3, 4, 5, 6]], b[:, [1, 3, 4, 5, 6]])
