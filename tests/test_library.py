@@ -2,6 +2,7 @@
 function include/ra.h declares, and rejects invalid requests before touching
 the device (no compute call is made here)."""
 import ctypes
+import os
 
 import pytest
 
@@ -146,3 +147,36 @@ def test_ulysses_validation_without_gpu():
     assert L.ra_forward_ulysses(Q, K, V, OUT, LSE, 1, 8, 4, 1024, 128, 4, 1, 0, None, 0, None) == \
         rb.RA_ERR_WORKSPACE
     assert L.ra_all_to_all(Q, K, 1, 6, 32, 8, 2, 4, 0, None) == rb.RA_ERR_INVALID_ARG   # Hn % n
+
+
+def test_header_is_plain_c_and_a_c_program_links(tmp_path):
+    """include/ra.h compiles as C99 (-pedantic, no C++), and a C program that
+    includes it links against libra.so and runs the host-only entry points."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    inc = os.path.join(root, "include")
+    libdir = os.path.dirname(ra.binding.LIB_PATH)
+    src = tmp_path / "use_ra.c"
+    src.write_text(
+        '#include <stdio.h>\n#include "ra.h"\n'
+        "int main(void) {\n"
+        "    long long pairs[16], tiles[16];\n"
+        "    long long total = ra_schedule_stats(RA_LAYOUT_STRIPED, 1, 4, 256, pairs, tiles);\n"
+        '    printf("%s|%s|%lld\\n", ra_version(), ra_status_string(RA_ERR_TIMEOUT), total);\n'
+        "    return total > 0 ? 0 : 1;\n"
+        "}\n")
+    exe = tmp_path / "use_ra"
+    res = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", inc, str(src),
+                          "-L", libdir, "-lra", "-Wl,-rpath," + libdir, "-o", str(exe)],
+                         capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert run.returncode == 0, run.stderr
+    version, timeout_name, total = run.stdout.strip().split("|")
+    assert version == ra.version() and "TIMEOUT" in timeout_name.upper()
+    S = 4 * 256
+    assert int(total) == S * (S + 1) // 2
