@@ -1,6 +1,8 @@
 // C-ABI layer of libra.so: argument validation, workspace layout, the host
 // ring-step scheduler, and the stream-ordered launch sequence.  See
 // include/ra.h for the contract of every entry point.
+#include <cstdio>
+#include <nvtx3/nvToolsExt.h>
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -23,6 +25,16 @@ namespace {
 constexpr unsigned long long kDefaultTimeoutNs = 4000000000ull;  // 4 s per wait
 unsigned long long g_timeout_ns = kDefaultTimeoutNs;
 std::atomic<unsigned long long> g_launches{0};
+// Host-side NVTX range around the enqueue of one phase (permute, attention,
+// ring step, merge, finalise).  A no-op unless a profiler or tracing tool is
+// attached; with one, timelines show the library's phases by name.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+
 // 0 automatic (= 3), 1 single-CTA, 2 CTA pair (cta_group::2), 3 single-CTA
 // kernel in clusters of two sharing each K/V load where the heads allow it
 std::atomic<int> g_kernel_variant{0};
@@ -318,8 +330,11 @@ ra_status forward_impl(const Problem &p, const void *q, const void *k, const voi
     char *base = static_cast<char *>(ws);
     const bool striped = p.layout == RA_LAYOUT_STRIPED && !p.rank_major;
     const long long row_bytes = (long long)p.d * (long long)p.esz();
+    NvtxRange r_call(p.mode == RA_MODE_FUSED ? "ra_forward (fused)"
+                     : p.mode == RA_MODE_RING ? "ra_forward (ring)" : "ra_forward (per step)");
     const void *qk = q, *kk = k, *vk = v;
     if (striped) {
+        NvtxRange r_perm("ra: permute q, k, v to rank-major");
         ra::launch_permute(q, base + w.q, (long long)p.B * p.H * p.S, p.S, p.N, row_bytes, 0, sm, st);
         ra::launch_permute(k, base + w.k, (long long)p.B * p.Hkv * p.S, p.S, p.N, row_bytes, 0, sm, st);
         ra::launch_permute(v, base + w.v, (long long)p.B * p.Hkv * p.S, p.S, p.N, row_bytes, 0, sm, st);
@@ -332,10 +347,14 @@ ra_status forward_impl(const Problem &p, const void *q, const void *k, const voi
     if (p.mode == RA_MODE_FUSED) {
         void *ok_out = striped ? (void *)(base + w.out) : out;
         float *ok_lse = striped ? (float *)(base + w.lse) : lse;
-        rs = attention_pass(p, qk, kk, vk, ok_out, ok_lse, 0, p.N, p.dtype == RA_DTYPE_F32, sm, st);
+        {
+            NvtxRange r_att("ra: attention, all ring steps");
+            rs = attention_pass(p, qk, kk, vk, ok_out, ok_lse, 0, p.N, p.dtype == RA_DTYPE_F32, sm, st);
+        }
         if (rs != RA_OK)
             return rs;
         if (striped) {
+            NvtxRange r_unperm("ra: out, lse back to natural order");
             ra::launch_permute(ok_out, out, (long long)p.rows(), p.S, p.N, row_bytes, 1, sm, st);
             ra::launch_permute(ok_lse, lse, (long long)p.rows(), p.S, p.N, 4, 1, sm, st);
             count_launch(2);
@@ -355,6 +374,9 @@ ra_status forward_impl(const Problem &p, const void *q, const void *k, const voi
     if (ring && (rs = rc.begin(p, kk, vk, base, w, st)) != RA_OK)
         return rs;
     for (int s = 0; s < p.N; ++s) {
+        char step_name[48];
+        snprintf(step_name, sizeof(step_name), "ra: ring step %d", s);
+        NvtxRange r_step(step_name);
         const void *ks = kk, *vs = vk;
         if (ring && (rs = rc.before_step(s, &ks, &vs, st)) != RA_OK)
             return rs;
@@ -376,6 +398,7 @@ ra_status forward_impl(const Problem &p, const void *q, const void *k, const voi
     }
     if (ring && (rs = rc.end(st)) != RA_OK)
         return rs;
+    NvtxRange r_fin("ra: finalise (divide, natural order)");
     ra::launch_finalize(run, run_lse, out, lse, p.dtype == RA_DTYPE_BF16, (long long)p.rows(), p.S,
                         p.N, striped ? 1 : 0, p.d, sm, st);
     count_launch();
@@ -494,6 +517,7 @@ ra_status backward_impl(const Problem &p, const void *q, const void *k, const vo
     const bool striped = p.layout == RA_LAYOUT_STRIPED;
     const long long row = (long long)p.d * (long long)p.esz();
     const long long qrows = (long long)p.B * p.H * p.S, kvrows = (long long)p.B * p.Hkv * p.S;
+    NvtxRange r_call("ra_backward");
     ra::BwdLaunch a{};
     a.q = q, a.k = k, a.v = v, a.out = out, a.dout = dout, a.lse = lse;
     a.dq = dq, a.dk = dk, a.dv = dv;
@@ -665,6 +689,7 @@ ra_status ra_forward_ulysses(const void *q, const void *k, const void *v, void *
     const int sm = sm_count_current();
     char *base = static_cast<char *>(ws);
     const long long row = (long long)d * pa.esz();
+    NvtxRange r_call("ra_forward_ulysses");
     // all-to-all in: every device gets all tokens of its heads
     ra::launch_all_to_all(q, base + w.q, B, H, S, n_dev, row, 0, sm, st);
     ra::launch_all_to_all(k, base + w.k, B, Hkv, S, n_dev, row, 0, sm, st);
