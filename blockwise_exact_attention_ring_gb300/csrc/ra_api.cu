@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 #include <vector>
 
@@ -60,6 +61,43 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb)
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// A caller buffer: its first byte and its size.
+struct Span {
+    const void *p;
+    size_t bytes;
+};
+
+// True when the first and the last byte of every buffer are device memory of
+// the current device.  The kernels' tensor maps (TMA copies, which the
+// default forward launch multicasts to both CTAs of a cluster) must cover
+// this GPU's own memory only, so pinned or plain host memory, managed memory
+// and a peer GPU's memory reached through unified addressing are refused.
+// Null pointers and empty buffers are skipped (the callers reject or allow
+// them before this check).
+bool resident_here(std::initializer_list<Span> bufs)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    for (const Span &b : bufs) {
+        if (!b.p || b.bytes == 0)
+            continue;
+        const char *first = static_cast<const char *>(b.p);
+        for (const char *x : {first, first + (b.bytes - 1)}) {
+            cudaPointerAttributes at{};
+            if (cudaPointerGetAttributes(&at, x) != cudaSuccess) {
+                cudaGetLastError();
+                return false;
+            }
+            if (at.type != cudaMemoryTypeDevice || at.device != dev)
+                return false;
+        }
+    }
+    return true;
+}
 
 struct Problem {
     int B, H, Hkv, S, d, N, layout, causal, dtype, mode;
@@ -306,12 +344,12 @@ struct RingCopies {
     }
 };
 
-ra_status forward_impl(const Problem &p, const void *q, const void *k, const void *v, void *out,
-                       float *lse, void *ws, size_t ws_bytes, cudaStream_t st)
+// Pointer checks shared by the forward entry points that take q, k, v, out
+// and lse in natural or rank-major order: non-null, 16-byte aligned, outputs
+// disjoint from the inputs and from each other.
+ra_status check_forward_ptrs(const Problem &p, const void *q, const void *k, const void *v, const void *out,
+                             const float *lse)
 {
-    ra_status rs = check_problem(p);
-    if (rs != RA_OK)
-        return rs;
     if (!q || !k || !v || !out || !lse)
         return RA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
@@ -322,8 +360,30 @@ ra_status forward_impl(const Problem &p, const void *q, const void *k, const voi
             return RA_ERR_INVALID_ARG;
     if (overlaps(out, qb, lse, lb))
         return RA_ERR_INVALID_ARG;
+    return RA_OK;
+}
+
+bool forward_resident(const Problem &p, const void *q, const void *k, const void *v, const void *out,
+                      const float *lse)
+{
+    const size_t qb = p.q_elems() * p.esz(), kvb = p.kv_elems() * p.esz(), lb = p.rows() * 4;
+    return resident_here({{q, qb}, {k, kvb}, {v, kvb}, {out, qb}, {lse, lb}});
+}
+
+ra_status forward_impl(const Problem &p, const void *q, const void *k, const void *v, void *out,
+                       float *lse, void *ws, size_t ws_bytes, cudaStream_t st, bool resident_checked = false)
+{
+    ra_status rs = check_problem(p);
+    if (rs != RA_OK)
+        return rs;
+    if ((rs = check_forward_ptrs(p, q, k, v, out, lse)) != RA_OK)
+        return rs;
     const WsLayout w = ws_layout(p);
     if (w.total > 0 && (!ws || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u)))
+        return RA_ERR_WORKSPACE;
+    if (!resident_checked && !forward_resident(p, q, k, v, out, lse))
+        return RA_ERR_INVALID_ARG;
+    if (w.total > 0 && !resident_here({{ws, w.total}}))
         return RA_ERR_WORKSPACE;
 
     const int sm = sm_count_current();
@@ -411,13 +471,17 @@ ra_status forward_alloc(const Problem &p, const void *q, const void *k, const vo
     ra_status rs = check_problem(p);
     if (rs != RA_OK)
         return rs;
+    if ((rs = check_forward_ptrs(p, q, k, v, out, lse)) != RA_OK)
+        return rs;
+    if (!forward_resident(p, q, k, v, out, lse))
+        return RA_ERR_INVALID_ARG;
     const size_t bytes = ws_layout(p).total;
     void *ws = nullptr;
     if (bytes > 0 && cudaMallocAsync(&ws, bytes, st) != cudaSuccess) {
         cudaGetLastError();
         return RA_ERR_NO_MEMORY;
     }
-    rs = forward_impl(p, q, k, v, out, lse, ws, bytes, st);
+    rs = forward_impl(p, q, k, v, out, lse, ws, bytes, st, true);
     if (ws && cudaFreeAsync(ws, st) != cudaSuccess && rs == RA_OK)
         rs = RA_ERR_CUDA;
     return rs;
@@ -511,6 +575,11 @@ ra_status backward_impl(const Problem &p, const void *q, const void *k, const vo
                 return RA_ERR_INVALID_ARG;
     const BwdWs w = bwd_ws_layout(p);
     if (!ws || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u))
+        return RA_ERR_WORKSPACE;
+    if (!resident_here({{q, qb}, {k, kvb}, {v, kvb}, {out, qb}, {lse, lb}, {dout, qb}, {dq, qb}, {dk, kvb},
+                        {dv, kvb}}))
+        return RA_ERR_INVALID_ARG;
+    if (!resident_here({{ws, w.total}}))
         return RA_ERR_WORKSPACE;
     const int sm = sm_count_current();
     char *base = static_cast<char *>(ws);
@@ -621,6 +690,8 @@ ra_status ra_forward_block(const void *q, const void *k, const void *v, float *o
             return RA_ERR_INVALID_ARG;
     if (overlaps(out_s, ob, lse_s, lb))
         return RA_ERR_INVALID_ARG;
+    if (!resident_here({{q, qb}, {k, kvb}, {v, kvb}, {out_s, ob}, {lse_s, lb}}))
+        return RA_ERR_INVALID_ARG;
     const int sm = sm_count_current();
     cudaStream_t st = (cudaStream_t)stream;
     const int j = ra_ring_block(rank, step, n_blocks);
@@ -649,6 +720,8 @@ ra_status ra_all_to_all(const void *src, void *dst, int B, int Hn, int S, int d,
         return RA_ERR_INVALID_ARG;
     const uintptr_t mis = (reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst));
     if ((row_bytes % 16 == 0 && (mis & 15u)) || (row_bytes % 4 == 0 && (mis & 3u)))
+        return RA_ERR_INVALID_ARG;
+    if (!resident_here({{src, total}, {dst, total}}))
         return RA_ERR_INVALID_ARG;
     ra::launch_all_to_all(src, dst, B, Hn, S, n_dev, row_bytes, inverse, sm_count_current(),
                           (cudaStream_t)stream);
@@ -684,6 +757,10 @@ ra_status ra_forward_ulysses(const void *q, const void *k, const void *v, void *
     if (overlaps(out, qb, lse, lb))
         return RA_ERR_INVALID_ARG;
     if (!ws || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u))
+        return RA_ERR_WORKSPACE;
+    if (!resident_here({{q, qb}, {k, kvb}, {v, kvb}, {out, qb}, {lse, lb}}))
+        return RA_ERR_INVALID_ARG;
+    if (!resident_here({{ws, w.total}}))
         return RA_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
     const int sm = sm_count_current();
@@ -849,6 +926,8 @@ ra_status ra_permute(const void *src, void *dst, int B, int Hn, int S, int d, in
     // vector width is chosen from the row size; pointers must match it
     if ((row_bytes % 16 == 0 && (mis & 15u)) || (row_bytes % 4 == 0 && (mis & 3u)))
         return RA_ERR_INVALID_ARG;
+    if (!resident_here({{src, total}, {dst, total}}))
+        return RA_ERR_INVALID_ARG;
     ra::launch_permute(src, dst, (long long)B * Hn * S, S, n_blocks, row_bytes, inverse,
                        sm_count_current(), (cudaStream_t)stream);
     count_launch();
@@ -867,6 +946,8 @@ ra_status ra_merge(float *out_run, float *lse_run, const float *out_s, const flo
     if (overlaps(out_run, ob, out_s, ob) || overlaps(lse_run, lb, lse_s, lb) ||
         overlaps(out_run, ob, lse_run, lb) || overlaps(out_run, ob, lse_s, lb) ||
         overlaps(lse_run, lb, out_s, ob))
+        return RA_ERR_INVALID_ARG;
+    if (!resident_here({{out_run, ob}, {lse_run, lb}, {out_s, ob}, {lse_s, lb}}))
         return RA_ERR_INVALID_ARG;
     ra::launch_merge(out_run, lse_run, out_s, lse_s, 1, rows, 0, rows, d, sm_count_current(),
                      (cudaStream_t)stream);
@@ -1007,16 +1088,9 @@ extern "C" ra_status ra_forward_noalloc(const void *q, const void *k, const void
     ra_status rs = check_problem(p);
     if (rs != RA_OK)
         return rs;
-    if (!q || !k || !v || !out || !lse)
-        return RA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
-        return RA_ERR_INVALID_ARG;
+    if ((rs = check_forward_ptrs(p, q, k, v, out, lse)) != RA_OK)
+        return rs;
     const size_t qb = p.q_elems() * p.esz(), kvb = p.kv_elems() * p.esz(), lb = p.rows() * 4;
-    for (const void *in : {q, k, v})
-        if (overlaps(out, qb, in, in == q ? qb : kvb) || overlaps(lse, lb, in, in == q ? qb : kvb))
-            return RA_ERR_INVALID_ARG;
-    if (overlaps(out, qb, lse, lb))
-        return RA_ERR_INVALID_ARG;
 
     // scratch (striped only): [q', k', v', out', lse'], 256-byte aligned
     const bool striped = layout == RA_LAYOUT_STRIPED;
@@ -1025,6 +1099,8 @@ extern "C" ra_status ra_forward_noalloc(const void *q, const void *k, const void
     const size_t need = striped ? off_l + align256(lb) : 0;
     if (need > RA_NOALLOC_SCRATCH_BYTES)
         return RA_ERR_SCRATCH_LIMIT;
+    if (!forward_resident(p, q, k, v, out, lse))
+        return RA_ERR_INVALID_ARG;
 
     char *base = nullptr;
     if (striped) {
@@ -1051,17 +1127,10 @@ extern "C" ra_status ra_forward_noalloc(const void *q, const void *k, const void
         ok_out = base + off_o;
         ok_lse = (float *)(base + off_l);
     }
-    ra::TcLaunch a{};
-    a.q = qk, a.k = kk, a.v = vk, a.out = ok_out, a.lse = ok_lse;
-    a.B = B, a.H = H, a.Hkv = Hkv, a.S = S, a.d = d, a.N = n_blocks;
-    a.layout = layout, a.causal = causal, a.s_begin = 0, a.s_end = n_blocks;
-    a.rank_lo = 0, a.rank_hi = n_blocks;
-    a.out_f32 = 0;
-    a.timeout_ns = g_timeout_ns;
-    a.sm_count = sm;
-    count_launch();
-    if (ra::launch_attn_tc(a, st) != cudaSuccess)
-        return RA_ERR_CUDA;
+    // the same kernel launch as ra_forward, including the kernel variant chosen
+    // with ra_set_kernel_variant
+    if ((rs = attention_pass(p, qk, kk, vk, ok_out, ok_lse, 0, n_blocks, false, sm, st)) != RA_OK)
+        return rs;
     if (striped) {
         ra::launch_permute(ok_out, out, (long long)p.rows(), S, n_blocks, row_bytes, 1, sm, st);
         ra::launch_permute(ok_lse, lse, (long long)p.rows(), S, n_blocks, 4, 1, sm, st);

@@ -582,14 +582,12 @@ cudaError_t launch_attn_pair(const TcLaunch &a, cudaStream_t st)
 {
     if (a.d != P_D)
         return cudaErrorInvalidValue;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(ra_attn_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             P_SMEM);
-        if (e != cudaSuccess)
-            return e;
-        attr_set = true;
-    }
+    static std::atomic<int> attr_set[RA_MAX_DEVICES];
+    cudaError_t e0 = once_per_device(attr_set, [] {
+        return cudaFuncSetAttribute(ra_attn_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
+    });
+    if (e0 != cudaSuccess)
+        return e0;
     PairParams p;
     memset(&p, 0, sizeof(p));
     const long long kv_rows = (long long)a.B * a.Hkv * a.S;

@@ -37,6 +37,7 @@
 //
 // TMEM columns: S/P tile 0 [0,128), S/P tile 1 [128,256), O tile 0
 // [256,256+d), O tile 1 [384,384+d).
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 #include <cuda.h>
@@ -628,42 +629,43 @@ bool encode_rows(CUtensorMap *tm, const void *base, long long rows, int d)
 template <int D, int CL>
 cudaError_t set_smem_attr()
 {
-    static bool done = false;
-    if (!done) {
-        cudaError_t e = cudaFuncSetAttribute(ra_attn_tc_kernel<D, CL>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
-        if (e != cudaSuccess)
-            return e;
-        done = true;
-    }
-    return cudaSuccess;
+    static std::atomic<int> done[RA_MAX_DEVICES];
+    return once_per_device(done, [] {
+        return cudaFuncSetAttribute(ra_attn_tc_kernel<D, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Cfg<D>::SMEM);
+    });
 }
 
-// Clusters of two that can be resident at once (one CTA per SM), queried once.
+// Clusters of two that can be resident at once on the current device (one
+// CTA per SM), queried once per device.
 template <int D>
 int max_pair_clusters()
 {
-    static int n = -1;
-    if (n < 0) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(2);
-        cfg.blockDim = dim3(NUM_THREADS);
-        cfg.dynamicSmemBytes = Cfg<D>::SMEM;
-        cudaLaunchAttribute at[1];
-        at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = 2;
-        at[0].val.clusterDim.y = 1;
-        at[0].val.clusterDim.z = 1;
-        cfg.attrs = at;
-        cfg.numAttrs = 1;
-        int c = 0;
-        if (cudaOccupancyMaxActiveClusters(&c, ra_attn_tc_kernel<D, 2>, &cfg) != cudaSuccess) {
-            cudaGetLastError();
-            c = 0;
-        }
-        n = c;
+    static std::atomic<int> known[RA_MAX_DEVICES];  // clusters + 1; 0 = not queried yet
+    const int dev = current_device_slot();
+    if (dev < 0)
+        return 0;
+    const int have = known[dev].load(std::memory_order_acquire);
+    if (have > 0)
+        return have - 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = Cfg<D>::SMEM;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int c = 0;
+    if (cudaOccupancyMaxActiveClusters(&c, ra_attn_tc_kernel<D, 2>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;  // not cached: asked again on the next launch
     }
-    return n;
+    known[dev].store(c + 1, std::memory_order_release);
+    return c;
 }
 
 template <int D>

@@ -783,18 +783,17 @@ template <int D>
 cudaError_t launch_bwd_d(const BwdLaunch &a, cudaStream_t st)
 {
     using C = BwdCfg<D>;
-    static bool attr_set = false;
-    if (!attr_set) {
+    static std::atomic<int> attr_set[RA_MAX_DEVICES];
+    cudaError_t e0 = once_per_device(attr_set, [] {
         cudaError_t e = cudaFuncSetAttribute(ra_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::KV_LAUNCH_SMEM);
         if (e != cudaSuccess)
             return e;
-        e = cudaFuncSetAttribute(ra_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::Q_LAUNCH_SMEM);
-        if (e != cudaSuccess)
-            return e;
-        attr_set = true;
-    }
+        return cudaFuncSetAttribute(ra_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    C::Q_LAUNCH_SMEM);
+    });
+    if (e0 != cudaSuccess)
+        return e0;
     const long long rows = (long long)a.B * a.H * a.S;
     {
         const long long threads = rows * (D / 8);

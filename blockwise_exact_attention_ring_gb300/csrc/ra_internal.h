@@ -2,6 +2,7 @@
 // translation units.  Not part of the public interface.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -12,6 +13,36 @@ namespace ra {
 
 // Status code the device error word carries for a bounded wait that ran out.
 constexpr unsigned int RA_DEV_TIMEOUT_CODE = 5;
+
+// One-time launch state (function attributes, occupancy queries) is kept per
+// device: a process that calls on several devices sets each device's up once.
+constexpr int RA_MAX_DEVICES = 64;
+
+// The current device, or -1 when it cannot be read or has no cache slot.
+inline int current_device_slot()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    return dev >= 0 && dev < RA_MAX_DEVICES ? dev : -1;
+}
+
+// Runs set_up() once per device (again after a failure); returns its error.
+template <class F>
+cudaError_t once_per_device(std::atomic<int> (&done)[RA_MAX_DEVICES], F set_up)
+{
+    const int dev = current_device_slot();
+    if (dev < 0)
+        return cudaErrorInvalidDevice;
+    if (done[dev].load(std::memory_order_acquire))
+        return cudaSuccess;
+    const cudaError_t e = set_up();
+    if (e == cudaSuccess)
+        done[dev].store(1, std::memory_order_release);
+    return e;
+}
 
 void launch_attn_f32(const float *q, const float *k, const float *v, float *out, float *lse,
                      int B, int H, int Hkv, int S, int d, int N, int layout, int causal,

@@ -37,6 +37,16 @@
  *   - Pointers are DEVICE pointers owned by the caller, 16-byte aligned, and
  *     stay valid until the enqueued work has finished.  `out` and `lse` must
  *     not overlap any input.
+ *   - Every buffer (inputs, outputs, caller workspace) must be device memory
+ *     of the CURRENT device: each call checks the first and last byte of each
+ *     one with cudaPointerGetAttributes and returns RA_ERR_INVALID_ARG
+ *     (RA_ERR_WORKSPACE for a workspace) for pinned or pageable host memory,
+ *     managed memory, or another GPU's memory reached through unified
+ *     addressing, before anything is enqueued.  The attention kernels load
+ *     tiles with TMA, and the default forward launch multicasts each
+ *     key/value tile to both CTAs of a cluster; those copies therefore only
+ *     ever read this GPU's own memory.  The library is meant for one process
+ *     on one GPU; it holds no multi-GPU code path.
  *   - Every call is asynchronous on `stream` (NULL = legacy default stream):
  *     it validates its arguments, enqueues kernels and returns.  A status
  *     other than RA_OK means nothing was enqueued and nothing was written.
@@ -286,7 +296,9 @@ ra_status ra_backward_ws(const void *q, const void *k, const void *v, const void
  * ra_forward_noalloc - ra_forward for callers that cannot allocate device
  * memory.  No counterpart on the pages: this is a deployment variant of the
  * same computation, with the same arguments, result and error rules as
- * ra_forward (bf16, fused ring, natural token order).
+ * ra_forward (bf16, fused ring, natural token order).  It enqueues the same
+ * kernels as ra_forward, including the forward kernel variant chosen with
+ * ra_set_kernel_variant, so its out and lse equal ra_forward's bit for bit.
  *
  * Who needs it: code that runs under a memory manager that owns every byte
  * of device memory (a framework's caching allocator or an inference server

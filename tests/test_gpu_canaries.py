@@ -4,7 +4,9 @@ call the sentinels must be intact bit for bit.  This stands in for a memory
 checker (closed on this pool) on the paths with ragged tails, where an
 off-by-one tile bound would write past the end: L not a multiple of 128,
 blocks shorter than a tile, one token per rank; both layouts, all forward
-modes, both dtypes, the CTA-pair launch, the backward and the permutation."""
+modes, both dtypes, every forward kernel variant (K/V-sharing clusters, one
+CTA, the CTA pair), the backward and the permutation.  The no-alloc entry
+point has its own guarded cases in the file that runs last."""
 import ctypes
 
 import pytest
@@ -61,6 +63,24 @@ def test_forward_writes_only_its_outputs(shape, layout, mode, dtype):
     lse = Guarded((B, H, S), torch.float32)
     ra.forward(q, k, v, n_blocks=N, layout=layout, causal=True, mode=mode, out=out.t, lse=lse.t)
     ra.check()
+    assert out.intact() and lse.intact()
+    assert torch.isfinite(out.t.float()).all() and torch.isfinite(lse.t).all()
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+@pytest.mark.parametrize("shape", RAGGED)
+@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+def test_every_forward_kernel_variant_writes_only_its_outputs(shape, layout, variant):
+    B, H, Hkv, S, d, N = shape
+    q, k, v = (t.cuda() for t in inputs.make_qkv(B, H, Hkv, S, d, seed=S + N + 17 * variant))
+    out = Guarded((B, H, S, d), torch.bfloat16)
+    lse = Guarded((B, H, S), torch.float32)
+    prev = ra.set_kernel_variant(variant)
+    try:
+        ra.forward(q, k, v, n_blocks=N, layout=layout, causal=True, out=out.t, lse=lse.t)
+        ra.check()
+    finally:
+        ra.set_kernel_variant(prev)
     assert out.intact() and lse.intact()
     assert torch.isfinite(out.t.float()).all() and torch.isfinite(lse.t).all()
 
