@@ -19,6 +19,11 @@ Matrix products are numpy float64 matmuls; nothing is blocked or reordered.
     1 drops delta, 2 uses dS instead of dS^T for dK (transposed operand),
     3 drops the scale of dK, 4 keeps only the first head of a GQA group in
     dK and dV, 5 masks keys u < t instead of u <= t.
+
+``dkdv_rows`` gives dK and dV for selected key rows only (the large
+workloads, where the full gradients do not fit a CPU check): for each key u
+it sums over the query rows t that see it, with every such row's softmax
+recomputed from scratch over all its visible keys.
 """
 from __future__ import annotations
 
@@ -112,3 +117,77 @@ def dq_rows(q, k, v, dout, rows, causal: bool = False) -> np.ndarray:
         ds = p * (dp - (p * dp).sum())
         out[n] = c * (ds @ kk)
     return out
+
+
+def dkdv_rows(q, k, v, dout, key_rows, causal: bool = False, fault: int = 0,
+              chunk_elems: int = 1 << 24) -> Tuple[np.ndarray, np.ndarray]:
+    """(dk, dv) [n, d] in fp64 for selected flattened (b, g, u) key rows of
+    the [B, Hkv, S, d] key/value tensors.  From the definition, per kv head g
+    and each query row (h, t) of its group that sees any selected key
+    (t >= u under the causal mask):
+
+        P[t, :]   = softmax over the visible keys of c q_t . k_u'
+        dP[t, u'] = dO_t . v_u'            delta_t = sum_u' P[t, u'] dP[t, u']
+        dV_u     += P[t, u] dO_t           dK_u   += c P[t, u] (dP[t, u] - delta_t) q_t
+
+    The query rows are taken in chunks of at most ``chunk_elems`` scores;
+    every chunk recomputes its rows' full softmax.  The arithmetic is plain
+    float64 PyTorch CPU ops (matmul, exp, sums), which use every host core.
+    ``fault`` plants the same kinds of mistakes as in ``attention_backward``
+    (pin tests only): 1 drops delta, 2 takes the query row at the key's
+    position (u) instead of t for dK, 3 drops the scale of dK, 4 keeps only
+    the first head of a GQA group, 5 hides key u from query u under the
+    causal mask."""
+    import torch
+
+    def f64(x):
+        return x.detach().cpu().double() if isinstance(x, torch.Tensor) else torch.from_numpy(_f64(x))
+
+    B, H, S, d = q.shape
+    Hkv = k.shape[1]
+    grp = H // Hkv
+    c = 1.0 / np.sqrt(d)
+    key_rows = np.asarray(key_rows, dtype=np.int64).ravel()
+    dk = torch.zeros(key_rows.size, d, dtype=torch.float64)
+    dv = torch.zeros(key_rows.size, d, dtype=torch.float64)
+    by_head = {}
+    for n, r in enumerate(key_rows):
+        b, g, u = int(r // (Hkv * S)), int(r // S % Hkv), int(r % S)
+        by_head.setdefault((b, g), []).append((n, u))
+    for (b, g), sel in by_head.items():
+        idx = torch.tensor([n for n, _ in sel])
+        us = torch.tensor([u for _, u in sel])
+        t_lo = int(us.min()) if causal else 0
+        kg, vg = f64(k[b, g]), f64(v[b, g])
+        vu = vg[us]
+        heads = range(grp) if fault != 4 else range(1)
+        step = max(1, chunk_elems // S)
+        for hh in heads:
+            h = g * grp + hh
+            qh, dh = f64(q[b, h]), f64(dout[b, h])
+            for t0 in range(t_lo, S, step):
+                t1 = min(S, t0 + step)
+                nk = t1 if causal else S          # keys any row of the chunk can see
+                qt, dt = qh[t0:t1], dh[t0:t1]
+                s = (qt @ kg[:nk].T) * c
+                if causal:
+                    t = torch.arange(t0, t1)[:, None]
+                    u_all = torch.arange(nk)[None, :]
+                    hidden = (u_all >= t) if fault == 5 else (u_all > t)
+                    if fault == 5:
+                        hidden[:, 0] = False      # keep every row defined
+                    s.masked_fill_(hidden, float("-inf"))
+                p = torch.softmax(s, dim=1)
+                dp = dt @ vg[:nk].T
+                delta = 0.0 if fault == 1 else (p * dp).sum(dim=1, keepdim=True)
+                vis = us < nk                     # selected keys inside the chunk's key range
+                pu = torch.zeros(t1 - t0, us.numel(), dtype=torch.float64)
+                pu[:, vis] = p[:, us[vis]]
+                dsu = pu * (dt @ vu.T - delta)
+                dv[idx] += pu.T @ dt
+                if fault == 2:
+                    part = dsu.sum(dim=0)[:, None] * qh[us]
+                else:
+                    part = dsu.T @ qt
+                dk[idx] += part if fault == 3 else c * part
+    return dk.numpy(), dv.numpy()

@@ -15,7 +15,7 @@ import torch
 
 import blockwise_exact_attention_ring_gb300 as ra
 from blockwise_exact_attention_ring_gb300 import inputs
-from oracle.backward import attention_backward, dq_rows
+from oracle.backward import attention_backward, dkdv_rows, dq_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -91,26 +91,48 @@ def test_backward_deterministic():
         assert torch.equal(x, y)
 
 
-@pytest.mark.parametrize("name", ["ring4-s32k-h32kv8-d128-causal-contiguous",
-                                  "ring8-s256k-h32kv8-d128-causal-striped"])
-def test_backward_workload_properties_and_sampled_rows(name):
-    """A workload's full shape (32K tokens over 4 blocks; 256K tokens over 8,
-    striped, as the bench's backward measurement runs): dq on sampled rows
-    against the oracle row by row, and over all keys the identities
-    sum_u dV = sum_t dO (per kv head) and sum_u dK = 0, which the whole dK and
-    dV must satisfy."""
+# Key rows compared element by element with the oracle at each workload size,
+# as (kv head, natural position) with S the sequence length.  Under the causal
+# mask key u is seen by the queries t >= u: early keys gather gradient from
+# the whole sequence (every ring step of every later block), late keys from a
+# few rows only (under striping the last positions belong to every rank).
+KEY_ROWS = {
+    "ring4-s32k-h32kv8-d128-causal-contiguous":
+        lambda S: [(0, 0), (0, 1), (0, 127), (0, 128), (0, 8191), (0, 8192),
+                   (5, S - 1), (5, S - 2), (5, S - 128), (5, S - 1000)],
+    "ring8-s256k-h32kv8-d128-causal-striped":
+        lambda S: [(g, S - o) for g in (0, 7) for o in (1, 2, 8, 9, 100, 257, 511, 512)],
+}
+
+
+@pytest.mark.parametrize("name", list(KEY_ROWS))
+def test_backward_workload_sampled_rows(name):
+    """A workload's full shape, in its own layout (32K tokens over 4
+    contiguous blocks; 256K tokens over 8, striped, as the bench's backward
+    measurement runs): dq on sampled query rows and dk, dv on sampled key rows
+    against the fp64 oracle row by row, each at the per-tensor bar
+    2e-2 * max |ref| over the compared rows; and over all keys the identities
+    sum_u dV = sum_t dO (per kv head) and sum_u dK = 0, which the whole dK
+    and dV must satisfy."""
     w = inputs.WORKLOADS[name]
-    layout = "striped"
+    layout = "striped" if w.layout == inputs.LAYOUT_STRIPED else "contiguous"
     q, k, v = inputs.workload_qkv(w, device="cuda")
     g = torch.Generator(device="cuda").manual_seed(77)
     dout = torch.randn(q.shape, generator=g, device="cuda").to(torch.bfloat16)
     out, lse = ra.forward(q, k, v, n_blocks=w.n_blocks, layout=layout, causal=True)
     dq, dk, dv = ra.backward(q, k, v, out, lse, dout, w.n_blocks, layout=layout, causal=True)
     ra.check()
+    qc, kc, vc, dc = (t.cpu() for t in (q, k, v, dout))
     rows = inputs.sample_rows(w.B, w.H, w.S, w.n_blocks, n=48 if w.S > 65536 else 96, seed=7)
-    ref = dq_rows(q.cpu(), k.cpu(), v.cpu(), dout.cpu(), rows, causal=True)
+    ref = dq_rows(qc, kc, vc, dc, rows, causal=True)
     got = dq.float().cpu().double().numpy().reshape(-1, w.d)[rows]
     assert np.abs(got - ref).max() <= REL_MAX * np.abs(ref).max()
+    key_rows = np.array([gg * w.S + u for gg, u in KEY_ROWS[name](w.S)])  # B = 1
+    ref_k, ref_v = dkdv_rows(qc, kc, vc, dc, key_rows, causal=True)
+    got_k = dk.float().cpu().double().numpy().reshape(-1, w.d)[key_rows]
+    got_v = dv.float().cpu().double().numpy().reshape(-1, w.d)[key_rows]
+    assert np.abs(got_k - ref_k).max() <= REL_MAX * np.abs(ref_k).max()
+    assert np.abs(got_v - ref_v).max() <= REL_MAX * np.abs(ref_v).max()
     grp = w.H // w.Hkv
     dv_sum = dv.double().sum(dim=2)
     do_sum = dout.double().reshape(w.B, w.Hkv, grp, w.S, w.d).sum(dim=(2, 3))

@@ -1,11 +1,13 @@
 """Pins of the fp64 backward oracle against things other than itself: torch
 autograd of the textbook formula, central finite differences, and two
-identities of the softmax gradient."""
+identities of the softmax gradient.  The sampled-key-row oracle dkdv_rows
+(used at workload sizes) is pinned against autograd directly, in chunks
+smaller than a row block so that the chunking is exercised too."""
 import numpy as np
 import pytest
 import torch
 
-from oracle.backward import attention_backward, dq_rows
+from oracle.backward import attention_backward, dkdv_rows, dq_rows
 
 
 def _inputs(B, H, Hkv, S, d, seed):
@@ -85,6 +87,41 @@ def test_backward_pins_pass():
 @pytest.mark.parametrize("fault", [1, 2, 3, 4, 5])
 def test_planted_backward_faults_are_caught(fault):
     assert not all(pin(fault) for pin in ALL_PINS), f"fault {fault} slipped through"
+
+
+def pin_rows_autograd(fault):
+    """dkdv_rows on chosen key rows (first, last, block edges, every kv head)
+    against torch autograd of the textbook formula."""
+    ok = True
+    for (B, H, Hkv, S, d), causal in [((1, 2, 1, 6, 4), True), ((2, 4, 2, 5, 3), False),
+                                      ((1, 4, 2, 9, 8), True), ((1, 3, 1, 11, 5), False)]:
+        q, k, v, do = _inputs(B, H, Hkv, S, d, seed=7 * S + d)
+        ks, vs = (t.clone().requires_grad_(True) for t in (k, v))
+        (_textbook_out(q, ks, vs, causal) * do).sum().backward()
+        rows = np.unique(np.array([0, 1, S // 2, S - 1, S, 2 * S - 1, B * Hkv * S - 1]) % (B * Hkv * S))
+        gk, gv = dkdv_rows(q, k, v, do, rows, causal, fault=fault, chunk_elems=2 * S)
+        ok &= bool(np.abs(gk - ks.grad.numpy().reshape(-1, d)[rows]).max() < 1e-10)
+        ok &= bool(np.abs(gv - vs.grad.numpy().reshape(-1, d)[rows]).max() < 1e-10)
+    return ok
+
+
+def test_dkdv_rows_pin_passes():
+    assert pin_rows_autograd(0)
+
+
+@pytest.mark.parametrize("fault", [1, 2, 3, 4, 5])
+def test_planted_dkdv_rows_faults_are_caught(fault):
+    assert not pin_rows_autograd(fault), f"fault {fault} slipped through"
+
+
+def test_dkdv_rows_match_full_oracle():
+    q, k, v, do = _inputs(2, 4, 2, 37, 8, seed=11)
+    for causal in (False, True):
+        _, dk, dv = attention_backward(q, k, v, do, causal)
+        rows = np.array([0, 3, 36, 37 + 5, 2 * 37 + 36, 3 * 37 + 17, 3 * 37 + 18])
+        gk, gv = dkdv_rows(q, k, v, do, rows, causal, chunk_elems=37 * 5)
+        assert np.abs(gk - dk.reshape(-1, 8)[rows]).max() < 1e-12
+        assert np.abs(gv - dv.reshape(-1, 8)[rows]).max() < 1e-12
 
 
 def test_dq_rows_match_full():
