@@ -368,9 +368,9 @@ def forward_ulysses(q, k, v, n_dev: int, causal: bool = False, workspace=None, s
 
 
 def set_kernel_variant(variant: int) -> int:
-    """0 automatic (= 3), 1 single-CTA, 2 CTA-pair tensor-core kernel, 3
-    single-CTA kernel in clusters of two sharing each key/value load where
-    the heads allow it; returns the previous setting."""
+    """0 automatic (= 3), 1 single-CTA tensor-core kernel, 3 single-CTA
+    kernel in clusters of two sharing each key/value load where the heads
+    allow it; returns the previous setting."""
     prev = lib().ra_set_kernel_variant(int(variant))
     if prev < 0:
         raise ValueError(f"invalid kernel variant {variant}")

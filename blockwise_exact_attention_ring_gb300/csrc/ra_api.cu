@@ -36,8 +36,8 @@ struct NvtxRange {
     NvtxRange &operator=(const NvtxRange &) = delete;
 };
 
-// 0 automatic (= 3), 1 single-CTA, 2 CTA pair (cta_group::2), 3 single-CTA
-// kernel in clusters of two sharing each K/V load where the heads allow it
+// 0 automatic (= 3), 1 single-CTA, 3 single-CTA kernel in clusters of two
+// sharing each K/V load where the heads allow it (2 is not a valid value)
 std::atomic<int> g_kernel_variant{0};
 
 void count_launch(unsigned long long n = 1) { g_launches.fetch_add(n, std::memory_order_relaxed); }
@@ -209,10 +209,8 @@ ra_status attention_pass(const Problem &p, const void *q, const void *k, const v
                                           rank_lo, rank_hi)) > 0)
         count_launch();
     const int variant = g_kernel_variant.load(std::memory_order_relaxed);
-    const bool pair = p.d == 128 && variant == 2;
-    a.cluster = (variant == 0 || variant == 3) ? 2 : 1;
-    return (pair ? ra::launch_attn_pair(a, st) : ra::launch_attn_tc(a, st)) == cudaSuccess ? RA_OK
-                                                                                         : RA_ERR_CUDA;
+    a.cluster = variant == 1 ? 1 : 2;
+    return ra::launch_attn_tc(a, st) == cudaSuccess ? RA_OK : RA_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------ ring copies
@@ -891,7 +889,7 @@ unsigned long long ra_launch_count(void) { return g_launches.load(std::memory_or
 
 int ra_set_kernel_variant(int variant)
 {
-    if (variant < 0 || variant > 3)
+    if (variant < 0 || variant > 3 || variant == 2)
         return -1;
     return g_kernel_variant.exchange(variant);
 }

@@ -45,6 +45,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include "ra_attn_common.cuh"
 #include "ra_internal.h"
 #include "ra_ptx_pair.cuh"
 
@@ -56,8 +57,6 @@ namespace {
 
 constexpr int NUM_THREADS = 384;  // 12 warps: TMA, MMA, 2 spare, 2 x 4 softmax
 constexpr uint32_t TMEM_COLS = 512;
-constexpr float LAZY_RESCALE_LOG2 = 8.0f;
-constexpr float LN2 = 0.693147180559945309f;
 
 enum Site : unsigned int {
     SITE_Q_EMPTY = 1, SITE_K_EMPTY, SITE_V_EMPTY, SITE_Q_FULL, SITE_K_FULL, SITE_V_FULL,
@@ -97,43 +96,6 @@ struct TcParams {
     float scale_log2;
     unsigned long long timeout_ns;
 };
-
-// Walks the key tiles of one unit in ring order: steps s in [s_begin, s_end),
-// block j = (i - s) mod N, tiles tb in [0, ra_kv_tiles(...)).
-struct KvWalk {
-    int i, N, layout, causal, ntiles, ta_max, s_end;
-    int s, j, cls, nt, tb;
-
-    __device__ void start(int rank, int tmax, const TcParams &p)
-    {
-        i = rank, N = p.N, layout = p.layout, causal = p.causal, ntiles = p.ntiles;
-        ta_max = tmax, s_end = p.s_end, s = p.s_begin - 1, j = 0, cls = 0, nt = 0;
-        next_block();
-    }
-    __device__ void next_block()
-    {
-        tb = 0;
-        while (++s < s_end) {
-            j = ra_ring_block(i, s, N);
-            cls = ra_block_class(layout, causal, i, j);
-            nt = ra_kv_tiles(cls, ta_max, ntiles);
-            if (nt > 0)
-                return;
-        }
-    }
-    __device__ bool valid() const { return s < s_end; }
-    __device__ void advance()
-    {
-        if (++tb >= nt)
-            next_block();
-    }
-};
-
-// Units are dealt to CTAs in snake order over the heaviest-first enumeration.
-__device__ __forceinline__ int unit_index(int round, int cta, int G)
-{
-    return round * G + ((round & 1) ? (G - 1 - cta) : cta);
-}
 
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int *abort,
                                           uint64_t timeout, unsigned int site)
@@ -180,89 +142,6 @@ __device__ __forceinline__ void load_tile_both(uint32_t dst, const CUtensorMap *
 #pragma unroll
     for (int h = 0; h < D / 64; ++h)
         tma_load_2d_mc(dst + h * Cfg<D>::SLAB, tm, h * 64, row, bar, (uint16_t)3, pol);
-}
-
-// One online-softmax step for the query row this thread owns.  The row's 128
-// scores of the current key tile are read from TMEM once (two 64-column
-// loads, one wait); on unmasked tiles the loads also return each half row's
-// maximum (tcgen05.ld.red), so no max pass over the registers is needed;
-// columns at or past `lim` count as -inf when MASK.  The
-// running max m (log2 domain, scores scaled by sl2 = log2e / sqrt(d)) only
-// moves when the tile max exceeds it by more than 2^8, and then O (in TMEM,
-// when has_o) and l are rescaled by 2^(m_old - m_new); the final division
-// cancels the common factor, so the result is exact.  P = 2^(s sl2 - m) is
-// packed to bf16 pairs over the first 64 columns of the tile (all scores are
-// in registers by then) for the P V MMA, and l accumulates the fp32 P.
-template <int D, bool MASK>
-__device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, int lim, float sl2, bool has_o,
-                                             float &m_run, float &l_run)
-{
-    const uint32_t ninf = __float_as_uint(-INFINITY);
-    float ma = -INFINITY, mb = -INFINITY;
-    uint32_t xa[64], xb[64];
-    if (MASK) {
-        tmem_ld64(tS, xa);
-        tmem_ld64(tS + 64, xb);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 64; ++e) {
-            xa[e] = e < lim ? xa[e] : ninf;
-            xb[e] = e + 64 < lim ? xb[e] : ninf;
-        }
-#pragma unroll
-        for (int e = 0; e < 64; e += 2) {
-            ma = max3f(ma, __uint_as_float(xa[e]), __uint_as_float(xa[e + 1]));
-            mb = max3f(mb, __uint_as_float(xb[e]), __uint_as_float(xb[e + 1]));
-        }
-    } else {
-        // the tensor-memory load reduces each half row to its maximum itself
-        tmem_ld64_max(tS, xa, ma);
-        tmem_ld64_max(tS + 64, xb, mb);
-        tmem_wait_ld();
-        asm volatile("" : "+f"(ma), "+f"(mb));  // keep every use of the maxima after the wait
-    }
-    const float m_tile = fmaxf(ma, mb) * sl2;  // -inf stays -inf
-    const bool resc = m_tile > m_run + LAZY_RESCALE_LOG2;
-    float alpha = 1.f;
-    if (resc) {
-        alpha = ex2_approx(m_run - m_tile);  // 0 when m_run = -inf
-        m_run = m_tile;
-        l_run *= alpha;
-    }
-    const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-    const float2 scale = make_float2(sl2, sl2), shift = make_float2(neg_m, neg_m);
-    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-            const uint32_t u0 = h ? xb[2 * e] : xa[2 * e];
-            const uint32_t u1 = h ? xb[2 * e + 1] : xa[2 * e + 1];
-            const float2 t2 = ffma2(make_float2(__uint_as_float(u0), __uint_as_float(u1)), scale, shift);
-            const float2 pv = make_float2(ex2_approx(t2.x), ex2_approx(t2.y));
-            if (e & 1)
-                acc1 = fadd2(acc1, pv);
-            else
-                acc0 = fadd2(acc0, pv);
-            pk[e] = pack_bf16x2(pv.x, pv.y);
-        }
-        tmem_st32(tS + h * 32, pk);
-    }
-    const float2 acc = fadd2(acc0, acc1);
-    l_run += acc.x + acc.y;
-    if (has_o && __any_sync(0xffffffffu, resc)) {
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-                o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(tO + c * 32, o);
-        }
-    }
 }
 
 // CL = 1: one CTA per SM.  CL = 2: clusters of two CTAs whose units have the
@@ -545,40 +424,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
                 break;
             ++ocnt;
             tc_fence_after();
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
             const bool valid = store && a < p.L;
             const long long orow = (long long)bh * p.S + (long long)U.rank * p.L + a;
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                __syncwarp();
-                tmem_ld32(tO + c * 32, o);
-                tmem_wait_ld();
-                if (!valid)
-                    continue;
-                if (p.out_f32) {
-                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + orow * D + c * 32);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv,
-                                             __uint_as_float(o[4 * e + 1]) * inv,
-                                             __uint_as_float(o[4 * e + 2]) * inv,
-                                             __uint_as_float(o[4 * e + 3]) * inv);
-                } else {
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + orow * D + c * 32);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        uint4 x;
-                        x.x = pack_bf16x2(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv);
-                        x.y = pack_bf16x2(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
-                        x.z = pack_bf16x2(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
-                        x.w = pack_bf16x2(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
-                        dst[e] = x;
-                    }
-                }
-            }
-            if (valid)
-                p.lse[orow] = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
+            store_row<D>(tO, valid, orow, m_run, l_run, p.out, p.lse, p.out_f32);
             __syncwarp();
             tc_fence_before();
             mbar_arrive(bar(ctrl->o_free[t]));

@@ -108,9 +108,6 @@ unsigned int *device_status_ptr();
 // or launching.
 cudaError_t launch_attn_tc(const TcLaunch &a, cudaStream_t st);
 
-// The same computation on clusters of two CTAs (cta_group::2); d = 128 only.
-cudaError_t launch_attn_pair(const TcLaunch &a, cudaStream_t st);
-
 // Device-side error word helpers (defined in ra_attn_sm103.cu).
 cudaError_t read_and_clear_device_status(unsigned int *status);
 

@@ -367,15 +367,14 @@ const char *ra_status_string(int status);
 /*
  * ra_set_kernel_variant - choose the bf16 tensor-core kernel for the calls
  * that follow (process-wide): 0 = automatic (the library's default choice,
- * currently variant 3),
- * 1 = one CTA per SM computing two 128-row query tiles, 2 = clusters of two
- * CTAs sharing each MMA (tcgen05 cta_group::2; head dimension 128 only, other
- * d use variant 1), 3 = variant 1 launched as clusters of two CTAs whose
- * units walk the same key/value tiles and share each tile load by TMA
- * multicast (when every kv head serves a multiple of four query heads;
- * otherwise variant 1).  All compute the same result (same ring order, same
- * running softmax); they differ in how work maps onto SMs.  Returns the
- * previous setting, or -1 for an invalid value (nothing changes).
+ * currently variant 3), 1 = one CTA per SM computing two 128-row query
+ * tiles, 3 = variant 1 launched as clusters of two CTAs whose units walk the
+ * same key/value tiles and share each tile load by TMA multicast (when every
+ * kv head serves a multiple of four query heads; otherwise variant 1).  Both
+ * compute the same result bit for bit (same ring order, same running
+ * softmax); they differ in how work maps onto SMs.  2 (a CTA-pair kernel in
+ * earlier versions) is no longer a valid value.  Returns the previous
+ * setting, or -1 for an invalid value (nothing changes).
  * Source: "Ring Attention" page, section "Halka Dikkati Nasil Calisir" (the
  * per-device blockwise kernel the ring runs).
  */

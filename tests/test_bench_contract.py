@@ -37,7 +37,7 @@ def test_gpu_arm_prints_one_contract_line():
     step's inputs and outputs through host memory."""
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "2", "--warmup", "3",
                           "--workload", "ring4-s32k-h32kv8-d128-causal-contiguous", "--no-cpu-baseline",
-                          "--no-backward"],
+                          "--no-backward", "--no-extra"],
                          capture_output=True, text=True, timeout=900, cwd=ROOT)
     assert out.returncode == 0, out.stderr[-2000:]
     lines = [l for l in out.stdout.splitlines() if l.strip()]
@@ -58,3 +58,13 @@ def test_gpu_arm_prints_one_contract_line():
     # the copies are inside the timed region: the end-to-end step cannot beat the device-resident one
     assert e["ms_per_step"] >= 0.98 * d["ms_per_step"]
     assert d["gpu_launches"] >= d["steps"]
+
+
+def test_gpus_other_than_one_are_refused():
+    """The bench measures on one GPU; a multi-GPU request is refused before
+    any work, with a message and exit status 2."""
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--steps", "1"],
+                         capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 2
+    assert out.stdout.strip() == ""
+    assert "one GPU" in out.stderr

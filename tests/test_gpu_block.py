@@ -97,33 +97,6 @@ def test_block_rejects_bad_arguments():
     ra.check()
 
 
-@pytest.mark.parametrize("layout,causal", [("contiguous", True), ("striped", True)])
-def test_block_partials_pair_kernel(layout, causal):
-    """The CTA-pair kernel (variant 2) restricted to one device's block gives
-    the same partials as the default kernel, up to bf16 rounding."""
-    B, H, Hkv, S, d, N = 1, 4, 2, 1024, 128, 4
-    L = S // N
-    q, k, v = inputs.make_qkv(B, H, Hkv, S, d, seed=33)
-    qd, kd, vd = (_rank_major(t.cuda().contiguous(), layout, N) for t in (q, k, v))
-    try:
-        for i, s in [(0, 0), (3, 1), (2, 2), (3, 3)]:
-            res = []
-            for variant in (1, 2):
-                ra.set_kernel_variant(variant)
-                out_s = torch.zeros(B, H, S, d, device="cuda")
-                lse_s = torch.zeros(B, H, S, device="cuda")
-                ra.forward_block(qd, kd, vd, out_s, lse_s, N, rank=i, step=s, layout=layout, causal=causal)
-                ra.check()
-                res.append((out_s[:, :, i * L:(i + 1) * L].clone(), lse_s[:, :, i * L:(i + 1) * L].clone()))
-            (o1, l1), (o2, l2) = res
-            fin = torch.isfinite(l1)
-            assert torch.equal(fin, torch.isfinite(l2))
-            assert (o1 - o2).abs().max().item() < 2e-2
-            assert (l1[fin] - l2[fin]).abs().max().item() < 1e-3
-    finally:
-        ra.set_kernel_variant(0)
-
-
 @pytest.mark.parametrize("layout", ["contiguous", "striped"])
 def test_merge_is_step_order_invariant(layout):
     """The ring's partials merged in ring order, reversed, and in a seeded

@@ -5,7 +5,7 @@ checker (closed on this pool) on the paths with ragged tails, where an
 off-by-one tile bound would write past the end: L not a multiple of 128,
 blocks shorter than a tile, one token per rank; both layouts, all forward
 modes, both dtypes, every forward kernel variant (K/V-sharing clusters, one
-CTA, the CTA pair), the backward and the permutation.  The no-alloc entry
+CTA), the backward and the permutation.  The no-alloc entry
 point has its own guarded cases in the file that runs last."""
 import ctypes
 
@@ -42,7 +42,7 @@ class Guarded:
 
 RAGGED = [
     # B, H, Hkv, S, d, N
-    (1, 8, 2, 600, 128, 3),    # L = 200: a full tile and a 72-row tail; group 4 (CTA pairs)
+    (1, 8, 2, 600, 128, 3),    # L = 200: a full tile and a 72-row tail; group 4 (CTA clusters)
     (1, 4, 2, 260, 64, 4),     # L = 65, d = 64, group 2
     (2, 8, 2, 32, 128, 4),     # L = 8, far below a tile
     (1, 4, 1, 4, 128, 4),      # L = 1: one token per rank
@@ -67,7 +67,7 @@ def test_forward_writes_only_its_outputs(shape, layout, mode, dtype):
     assert torch.isfinite(out.t.float()).all() and torch.isfinite(lse.t).all()
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+@pytest.mark.parametrize("variant", [0, 1, 3])
 @pytest.mark.parametrize("shape", RAGGED)
 @pytest.mark.parametrize("layout", ["contiguous", "striped"])
 def test_every_forward_kernel_variant_writes_only_its_outputs(shape, layout, variant):
