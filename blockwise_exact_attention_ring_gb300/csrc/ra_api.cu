@@ -44,6 +44,9 @@ void count_launch(unsigned long long n = 1) { g_launches.fetch_add(n, std::memor
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Largest number of pieces a unit's ring walk is split into (split_count).
+constexpr int kMaxSplit = 16;
+
 int sm_count_current()
 {
     int dev = 0, n = 0;
@@ -68,13 +71,14 @@ struct Span {
     size_t bytes;
 };
 
-// True when the first and the last byte of every buffer are device memory of
-// the current device.  The kernels' tensor maps (TMA copies, which the
-// default forward launch multicasts to both CTAs of a cluster) must cover
-// this GPU's own memory only, so pinned or plain host memory, managed memory
-// and a peer GPU's memory reached through unified addressing are refused.
-// Null pointers and empty buffers are skipped (the callers reject or allow
-// them before this check).
+// True when every buffer starts in device memory of the current device.
+// The kernels' tensor maps (TMA copies, which the default forward launch
+// multicasts to both CTAs of a cluster) must cover this GPU's own memory
+// only, so pinned or plain host memory, managed memory and a peer GPU's
+// memory reached through unified addressing are refused.  One
+// cudaPointerGetAttributes per buffer (its first byte: an allocation lies in
+// one memory).  Null pointers and empty buffers are skipped (the callers
+// reject or allow them before this check).
 bool resident_here(std::initializer_list<Span> bufs)
 {
     int dev = 0;
@@ -85,16 +89,13 @@ bool resident_here(std::initializer_list<Span> bufs)
     for (const Span &b : bufs) {
         if (!b.p || b.bytes == 0)
             continue;
-        const char *first = static_cast<const char *>(b.p);
-        for (const char *x : {first, first + (b.bytes - 1)}) {
-            cudaPointerAttributes at{};
-            if (cudaPointerGetAttributes(&at, x) != cudaSuccess) {
-                cudaGetLastError();
-                return false;
-            }
-            if (at.type != cudaMemoryTypeDevice || at.device != dev)
-                return false;
+        cudaPointerAttributes at{};
+        if (cudaPointerGetAttributes(&at, b.p) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
         }
+        if (at.type != cudaMemoryTypeDevice || at.device != dev)
+            return false;
     }
     return true;
 }
@@ -137,20 +138,47 @@ ra_status check_problem(const Problem &p)
     return RA_OK;
 }
 
+// Pieces the fused bf16 kernel cuts every unit's walk over its key tiles
+// into.  The ring's own decomposition: the key tiles a query tile meets are
+// independent partial results that the running softmax combines, so when the
+// work units cannot fill half the SMs, each unit's walk (in ring order) is
+// split into up to sm / units contiguous pieces, computed by different CTAs
+// and combined afterwards.  1 otherwise (and for the fp32 and per-step paths).
+int split_count(const Problem &p, int sm)
+{
+    if (p.mode != RA_MODE_FUSED || p.dtype != RA_DTYPE_BF16)
+        return 1;
+    const RaUnitSpace sp = ra_unit_space(p.B, p.H, p.Hkv, p.S, p.N, p.layout, p.causal, 0, p.N);
+    const long long units = ra_unit_count(sp);
+    if (units < 1 || 2 * units > sm)
+        return 1;
+    const int heaviest = ra_unit_decode(sp, 0).cost;  // the order is heaviest first
+    long long n = sm / units;
+    if (n > kMaxSplit)
+        n = kMaxSplit;
+    if (n > heaviest)
+        n = heaviest;
+    return n > 1 ? (int)n : 1;
+}
+
 // Workspace layout (each region 256-byte aligned):
 //   striped:            q', k', v' in striped order
-//   striped and fused:  out', lse' in striped order
+//   striped and fused:  out', lse' in striped order (unless split)
+//   fused, split:       nsplit fp32 partials of out and lse (kernel order)
 //   per-step and ring:  running out/lse (fp32) and step partial out/lse (fp32)
 //   ring:               two rotating copies of k and v (rank-major order)
 struct WsLayout {
     size_t q = 0, k = 0, v = 0, out = 0, lse = 0, run = 0, run_lse = 0, part = 0, part_lse = 0;
     size_t ring_k[2] = {0, 0}, ring_v[2] = {0, 0};
+    size_t split = 0, split_lse = 0;
+    int nsplit = 1;
     size_t total = 0;
 };
 
-WsLayout ws_layout(const Problem &p)
+WsLayout ws_layout(const Problem &p, int sm)
 {
     WsLayout w;
+    w.nsplit = split_count(p, sm);
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t at = off;
@@ -161,10 +189,14 @@ WsLayout ws_layout(const Problem &p)
         w.q = take(p.q_elems() * p.esz());
         w.k = take(p.kv_elems() * p.esz());
         w.v = take(p.kv_elems() * p.esz());
-        if (p.mode == RA_MODE_FUSED) {
+        if (p.mode == RA_MODE_FUSED && w.nsplit == 1) {
             w.out = take(p.q_elems() * p.esz());
             w.lse = take(p.rows() * 4);
         }
+    }
+    if (w.nsplit > 1) {
+        w.split = take((size_t)w.nsplit * p.q_elems() * 4);
+        w.split_lse = take((size_t)w.nsplit * p.rows() * 4);
     }
     if (p.mode != RA_MODE_FUSED) {
         w.run = take(p.q_elems() * 4);
@@ -185,7 +217,7 @@ WsLayout ws_layout(const Problem &p)
 // ------------------------------------------------------------------ forward
 ra_status attention_pass(const Problem &p, const void *q, const void *k, const void *v, void *out,
                          float *lse, int s_begin, int s_end, bool out_f32, int sm, cudaStream_t st,
-                         int rank_lo = 0, int rank_hi = -1)
+                         int rank_lo = 0, int rank_hi = -1, int nsplit = 1)
 {
     if (rank_hi < 0)
         rank_hi = p.N;
@@ -204,6 +236,9 @@ ra_status attention_pass(const Problem &p, const void *q, const void *k, const v
     a.out_f32 = out_f32 ? 1 : 0;
     a.timeout_ns = g_timeout_ns;
     a.sm_count = sm;
+    a.nsplit = nsplit;
+    a.split_out_bytes = (long long)p.q_elems() * 4;
+    a.split_lse_stride = (long long)p.rows();
     if (ra_unit_count(ra_unit_space_ranks(ra_unit_space(p.B, p.H, p.Hkv, p.S, p.N, p.layout, p.causal,
                                                         s_begin, s_end),
                                           rank_lo, rank_hi)) > 0)
@@ -368,23 +403,27 @@ bool forward_resident(const Problem &p, const void *q, const void *k, const void
     return resident_here({{q, qb}, {k, kvb}, {v, kvb}, {out, qb}, {lse, lb}});
 }
 
+// resident_checked: the caller has checked that q, k, v, out and lse are
+// device memory of the current device; ws_internal: ws is the library's own
+// scratch array (no residency check needed).
 ra_status forward_impl(const Problem &p, const void *q, const void *k, const void *v, void *out,
-                       float *lse, void *ws, size_t ws_bytes, cudaStream_t st, bool resident_checked = false)
+                       float *lse, void *ws, size_t ws_bytes, cudaStream_t st, bool resident_checked = false,
+                       bool ws_internal = false)
 {
     ra_status rs = check_problem(p);
     if (rs != RA_OK)
         return rs;
     if ((rs = check_forward_ptrs(p, q, k, v, out, lse)) != RA_OK)
         return rs;
-    const WsLayout w = ws_layout(p);
+    const int sm = sm_count_current();
+    const WsLayout w = ws_layout(p, sm);
     if (w.total > 0 && (!ws || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u)))
         return RA_ERR_WORKSPACE;
     if (!resident_checked && !forward_resident(p, q, k, v, out, lse))
         return RA_ERR_INVALID_ARG;
-    if (w.total > 0 && !resident_here({{ws, w.total}}))
+    if (w.total > 0 && !ws_internal && !resident_here({{ws, w.total}}))
         return RA_ERR_WORKSPACE;
 
-    const int sm = sm_count_current();
     char *base = static_cast<char *>(ws);
     const bool striped = p.layout == RA_LAYOUT_STRIPED && !p.rank_major;
     const long long row_bytes = (long long)p.d * (long long)p.esz();
@@ -402,6 +441,21 @@ ra_status forward_impl(const Problem &p, const void *q, const void *k, const voi
         qk = base + w.q, kk = base + w.k, vk = base + w.v;
     }
 
+    if (p.mode == RA_MODE_FUSED && w.nsplit > 1) {
+        {
+            NvtxRange r_att("ra: attention, all ring steps, walks split into pieces");
+            rs = attention_pass(p, qk, kk, vk, base + w.split, (float *)(base + w.split_lse), 0, p.N, true, sm,
+                                st, 0, -1, w.nsplit);
+        }
+        if (rs != RA_OK)
+            return rs;
+        NvtxRange r_comb("ra: combine the pieces (natural order)");
+        ra::launch_combine((const float *)(base + w.split), (const float *)(base + w.split_lse), w.nsplit,
+                           (long long)p.rows(), out, lse, 1, (long long)p.rows(), p.S, p.N, striped ? 1 : 0,
+                           p.d, sm, st);
+        count_launch();
+        return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+    }
     if (p.mode == RA_MODE_FUSED) {
         void *ok_out = striped ? (void *)(base + w.out) : out;
         float *ok_lse = striped ? (float *)(base + w.lse) : lse;
@@ -473,7 +527,7 @@ ra_status forward_alloc(const Problem &p, const void *q, const void *k, const vo
         return rs;
     if (!forward_resident(p, q, k, v, out, lse))
         return RA_ERR_INVALID_ARG;
-    const size_t bytes = ws_layout(p).total;
+    const size_t bytes = ws_layout(p, sm_count_current()).total;
     void *ws = nullptr;
     if (bytes > 0 && cudaMallocAsync(&ws, bytes, st) != cudaSuccess) {
         cudaGetLastError();
@@ -647,7 +701,7 @@ size_t ra_workspace_bytes(int B, int H, int Hkv, int S, int d, int n_blocks, int
     const Problem p{B, H, Hkv, S, d, n_blocks, layout, causal, dtype, mode};
     if (check_problem(p) != RA_OK)
         return 0;
-    return ws_layout(p).total;
+    return ws_layout(p, sm_count_current()).total;
 }
 
 ra_status ra_forward_ws(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
@@ -1088,53 +1142,15 @@ extern "C" ra_status ra_forward_noalloc(const void *q, const void *k, const void
         return rs;
     if ((rs = check_forward_ptrs(p, q, k, v, out, lse)) != RA_OK)
         return rs;
-    const size_t qb = p.q_elems() * p.esz(), kvb = p.kv_elems() * p.esz(), lb = p.rows() * 4;
-
-    // scratch (striped only): [q', k', v', out', lse'], 256-byte aligned
-    const bool striped = layout == RA_LAYOUT_STRIPED;
-    const size_t off_q = 0, off_k = off_q + align256(qb), off_v = off_k + align256(kvb);
-    const size_t off_o = off_v + align256(kvb), off_l = off_o + align256(qb);
-    const size_t need = striped ? off_l + align256(lb) : 0;
+    // the workspace ra_forward would allocate, taken from the fixed array
+    const size_t need = ws_layout(p, sm_count_current()).total;
     if (need > RA_NOALLOC_SCRATCH_BYTES)
         return RA_ERR_SCRATCH_LIMIT;
     if (!forward_resident(p, q, k, v, out, lse))
         return RA_ERR_INVALID_ARG;
-
-    char *base = nullptr;
-    if (striped) {
-        void *scratch = nullptr;
-        if ((rs = noalloc_scratch(&scratch)) != RA_OK)
-            return rs;
-        base = static_cast<char *>(scratch);
-    }
-    cudaStream_t st = (cudaStream_t)stream;
-
-    const int sm = sm_count_current();
-    const long long row_bytes = (long long)d * 2;
-    const void *qk = q, *kk = k, *vk = v;
-    void *ok_out = out;
-    float *ok_lse = lse;
-    if (striped) {
-        ra::launch_permute(q, base + off_q, (long long)B * H * S, S, n_blocks, row_bytes, 0, sm, st);
-        ra::launch_permute(k, base + off_k, (long long)B * Hkv * S, S, n_blocks, row_bytes, 0, sm, st);
-        ra::launch_permute(v, base + off_v, (long long)B * Hkv * S, S, n_blocks, row_bytes, 0, sm, st);
-        count_launch(3);
-        if (cudaGetLastError() != cudaSuccess)
-            return RA_ERR_CUDA;
-        qk = base + off_q, kk = base + off_k, vk = base + off_v;
-        ok_out = base + off_o;
-        ok_lse = (float *)(base + off_l);
-    }
-    // the same kernel launch as ra_forward, including the kernel variant chosen
-    // with ra_set_kernel_variant
-    if ((rs = attention_pass(p, qk, kk, vk, ok_out, ok_lse, 0, n_blocks, false, sm, st)) != RA_OK)
+    void *scratch = nullptr;
+    if (need > 0 && (rs = noalloc_scratch(&scratch)) != RA_OK)
         return rs;
-    if (striped) {
-        ra::launch_permute(ok_out, out, (long long)p.rows(), S, n_blocks, row_bytes, 1, sm, st);
-        ra::launch_permute(ok_lse, lse, (long long)p.rows(), S, n_blocks, 4, 1, sm, st);
-        count_launch(2);
-        if (cudaGetLastError() != cudaSuccess)
-            return RA_ERR_CUDA;
-    }
-    return RA_OK;
+    // the same enqueue as ra_forward, on the library's array
+    return forward_impl(p, q, k, v, out, lse, scratch, need, (cudaStream_t)stream, true, true);
 }

@@ -52,6 +52,19 @@ struct KvWalk {
         if (++tb >= nt)
             next_block();
     }
+    // Moves n key tiles ahead along the walk (a block at a time).
+    __device__ void skip(int n)
+    {
+        while (n > 0 && valid()) {
+            const int left = nt - tb;
+            if (n < left) {
+                tb += n;
+                return;
+            }
+            n -= left;
+            next_block();
+        }
+    }
 };
 
 // Units are dealt to CTAs (or clusters) in snake order over the

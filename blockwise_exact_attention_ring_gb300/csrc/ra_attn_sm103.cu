@@ -92,10 +92,39 @@ struct TcParams {
     RaUnitSpace sp;  // the launch's work units, decoded on the fly
     void *out;
     float *lse;
-    int n_units, H, Hkv, S, L, N, layout, causal, s_begin, s_end, out_f32, ntiles;
+    int n_items, H, Hkv, S, L, N, layout, causal, s_begin, s_end, out_f32, ntiles;
+    // Work items: unit u, piece k of its key tiles in ring order.  nsplit = 1:
+    // one item per unit (the whole walk).  nsplit > 1: item k of a unit walks
+    // tiles [k c / nsplit, (k + 1) c / nsplit) of its c tiles and writes its
+    // own fp32 partial at out + k split_out_bytes, lse + k split_lse_stride.
+    // pair_items keeps the items of units 2m and 2m + 1 next to each other.
+    int nsplit, pair_items;
+    long long split_out_bytes, split_lse_stride;
     float scale_log2;
     unsigned long long timeout_ns;
 };
+
+// Work item w: its unit's description, piece index k and tile range
+// [t0, t0 + cnt).
+__device__ __forceinline__ RaUnit item_decode(const TcParams &p, int w, int &k, int &t0, int &cnt)
+{
+    int u = w;
+    k = 0;
+    if (p.nsplit > 1) {
+        if (p.pair_items) {
+            const int m = w / (2 * p.nsplit), rem = w - m * 2 * p.nsplit;
+            k = rem >> 1;
+            u = 2 * m + (rem & 1);
+        } else {
+            u = w / p.nsplit;
+            k = w - u * p.nsplit;
+        }
+    }
+    const RaUnit U = ra_unit_decode(p.sp, u);
+    t0 = (int)((long long)k * U.cost / p.nsplit);
+    cnt = (int)((long long)(k + 1) * U.cost / p.nsplit) - t0;
+    return U;
+}
 
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int *abort,
                                           uint64_t timeout, unsigned int site)
@@ -150,7 +179,7 @@ __device__ __forceinline__ void load_tile_both(uint32_t dst, const CUtensorMap *
 // loads each K tile and CTA 1 each V tile into BOTH CTAs' shared memory by
 // TMA multicast, and a stage is reloaded only after both CTAs' MMAs have
 // consumed it (each MMA warp commits to the empty barrier of both CTAs).
-template <int D, int CL>
+template <int D, int CL, bool SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid_constant__ TcParams p)
 {
     using C = Cfg<D>;
@@ -225,10 +254,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
             uint32_t kcnt = 0, vcnt = 0, qcnt = 0;
             bool ok = true;
             for (int r = 0; ok; ++r) {
-                const int u = unit_of(r);
-                if (u >= p.n_units)
+                const int wi = unit_of(r);
+                if (wi >= p.n_items)
                     break;
-                const RaUnit U = ra_unit_decode(p.sp, u);
+                int k = 0, t0 = 0, cnt = 0;
+                const RaUnit U = SPLIT ? item_decode(p, wi, k, t0, cnt) : ra_unit_decode(p.sp, wi);
+                if (SPLIT && cnt == 0)
+                    continue;  // an empty piece: nothing to load
                 if (qcnt > 0 && !(ok = wait1(bar(ctrl->q_empty), (qcnt - 1) & 1, abort, tmo,
                                                  SITE_Q_EMPTY)))
                     break;
@@ -242,7 +274,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
                 const int kvbh = b * p.Hkv + (U.bh0 - b * p.H) / group;
                 KvWalk w;
                 w.start(U.rank, max(U.ta0, U.ta1), p);
-                for (; w.valid(); w.advance()) {
+                if (SPLIT)
+                    w.skip(t0);
+                for (int c = 0; SPLIT ? c < cnt : w.valid(); ++c, w.advance()) {
                     const int row = kvbh * p.S + w.j * p.L + w.tb * RA_TILE;
                     const int ks = kcnt % C::KSTAGES;
                     if (!(ok = kv_wait(bar(ctrl->k_empty[ks]), ((kcnt / C::KSTAGES) & 1) ^ 1,
@@ -307,10 +341,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
             uint32_t kcnt = 0, vcnt = 0, qcnt = 0, pcnt = 0;
             bool ok = true;
             for (int r = 0; ok; ++r) {
-                const int u = unit_of(r);
-                if (u >= p.n_units)
+                const int wi = unit_of(r);
+                if (wi >= p.n_items)
                     break;
-                const int n = ra_unit_decode(p.sp, u).cost;
+                int k = 0, t0 = 0, n = 0;
+                if (SPLIT)
+                    item_decode(p, wi, k, t0, n);
+                else
+                    n = ra_unit_decode(p.sp, wi).cost;
+                if (SPLIT && n == 0)
+                    continue;  // an empty piece: no MMA
                 if (!(ok = wait1(bar(ctrl->q_full), qcnt & 1, abort, tmo, SITE_Q_FULL)))
                     break;
                 int ks = kcnt % C::KSTAGES;
@@ -384,18 +424,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
         uint32_t scnt = 0, ocnt = 0;
         bool ok = true;
         for (int rr = 0; ok; ++rr) {
-            const int u = unit_of(rr);
-            if (u >= p.n_units)
+            const int wi = unit_of(rr);
+            if (wi >= p.n_items)
                 break;
-            const RaUnit U = ra_unit_decode(p.sp, u);
+            int k = 0, t0 = 0, cnt = 0;
+            const RaUnit U = SPLIT ? item_decode(p, wi, k, t0, cnt) : ra_unit_decode(p.sp, wi);
             const int bh = t ? U.bh1 : U.bh0;
             const int ta = t ? U.ta1 : U.ta0;
             const bool store = (t == 0) || U.tile1_valid;
             const int a = ta * RA_TILE + r;
+            if (SPLIT && cnt == 0) {
+                // an empty piece: its partial holds no key (lse = -inf)
+                if (store && a < p.L)
+                    p.lse[k * p.split_lse_stride + (long long)bh * p.S + (long long)U.rank * p.L + a] = -INFINITY;
+                continue;
+            }
             float m_run = -INFINITY, l_run = 0.f;
             KvWalk w;
             w.start(U.rank, max(U.ta0, U.ta1), p);
-            for (int jj = 0; w.valid(); w.advance(), ++jj) {
+            if (SPLIT)
+                w.skip(t0);
+            for (int jj = 0; SPLIT ? jj < cnt : w.valid(); w.advance(), ++jj) {
                 if (!(ok = wait_warp(bar(ctrl->s_full[t]), scnt & 1, abort, tmo, SITE_S_FULL)))
                     break;
                 ++scnt;
@@ -426,7 +475,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
             tc_fence_after();
             const bool valid = store && a < p.L;
             const long long orow = (long long)bh * p.S + (long long)U.rank * p.L + a;
-            store_row<D>(tO, valid, orow, m_run, l_run, p.out, p.lse, p.out_f32);
+            if (SPLIT)
+                store_row<D>(tO, valid, orow, m_run, l_run, static_cast<char *>(p.out) + k * p.split_out_bytes,
+                             p.lse + k * p.split_lse_stride, 1);
+            else
+                store_row<D>(tO, valid, orow, m_run, l_run, p.out, p.lse, p.out_f32);
             __syncwarp();
             tc_fence_before();
             mbar_arrive(bar(ctrl->o_free[t]));
@@ -474,12 +527,12 @@ bool encode_rows(CUtensorMap *tm, const void *base, long long rows, int d)
     return r == CUDA_SUCCESS;
 }
 
-template <int D, int CL>
+template <int D, int CL, bool SPLIT>
 cudaError_t set_smem_attr()
 {
     static std::atomic<int> done[RA_MAX_DEVICES];
     return once_per_device(done, [] {
-        return cudaFuncSetAttribute(ra_attn_tc_kernel<D, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        return cudaFuncSetAttribute(ra_attn_tc_kernel<D, CL, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     Cfg<D>::SMEM);
     });
 }
@@ -508,7 +561,7 @@ int max_pair_clusters()
     cfg.attrs = at;
     cfg.numAttrs = 1;
     int c = 0;
-    if (cudaOccupancyMaxActiveClusters(&c, ra_attn_tc_kernel<D, 2>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&c, ra_attn_tc_kernel<D, 2, false>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;  // not cached: asked again on the next launch
     }
@@ -516,48 +569,21 @@ int max_pair_clusters()
     return c;
 }
 
-template <int D>
-cudaError_t launch_d(const TcLaunch &a, cudaStream_t st)
+// One launch of the kernel: clusters of two (CL = 2) or one CTA per SM.
+template <int D, bool SPLIT>
+cudaError_t launch_grid(const TcParams &p, bool clusters, int sm_count, cudaStream_t st)
 {
     using C = Cfg<D>;
-    cudaError_t e = set_smem_attr<D, 1>();
-    if (e != cudaSuccess)
-        return e;
-    TcParams p;
-    memset(&p, 0, sizeof(p));
-    if (!encode_rows(&p.tm_q, a.q, (long long)a.B * a.H * a.S, D) ||
-        !encode_rows(&p.tm_k, a.k, (long long)a.B * a.Hkv * a.S, D) ||
-        !encode_rows(&p.tm_v, a.v, (long long)a.B * a.Hkv * a.S, D))
-        return cudaErrorInvalidValue;
-    p.sp = ra_unit_space_ranks(ra_unit_space(a.B, a.H, a.Hkv, a.S, a.N, a.layout, a.causal, a.s_begin, a.s_end),
-                               a.rank_lo, a.rank_hi);
-    const long long n_units = ra_unit_count(p.sp);
-    if (n_units > 0x7fffffffll)
-        return cudaErrorInvalidValue;
-    p.out = a.out;
-    p.lse = a.lse;
-    p.n_units = (int)n_units;
-    p.H = a.H, p.Hkv = a.Hkv, p.S = a.S, p.N = a.N, p.L = a.S / a.N;
-    p.layout = a.layout, p.causal = a.causal;
-    p.s_begin = a.s_begin, p.s_end = a.s_end, p.out_f32 = a.out_f32;
-    p.ntiles = (p.L + RA_TILE - 1) / RA_TILE;
-    p.scale_log2 = 1.4426950408889634f / sqrtf((float)D);
-    p.timeout_ns = a.timeout_ns;
-    if (p.n_units <= 0)
-        return cudaSuccess;
-    // Clusters need units (2m, 2m + 1) with one key/value walk: two head
-    // pairs of one kv head next to each other in the order, i.e. an even
-    // number of head pairs per kv head.
-    const int pairs_per_kv = p.sp.head_pairs ? (a.H / a.Hkv) / 2 : 0;
-    if (a.cluster == 2 && pairs_per_kv >= 2 && pairs_per_kv % 2 == 0 && p.n_units % 2 == 0) {
-        if ((e = set_smem_attr<D, 2>()) != cudaSuccess)
+    cudaError_t e;
+    if (clusters) {
+        if ((e = set_smem_attr<D, 2, SPLIT>()) != cudaSuccess)
             return e;
         const int max_cl = max_pair_clusters<D>();
         if (max_cl >= 1) {
-            const int pairs = p.n_units / 2;
-            const int clusters = pairs < max_cl ? pairs : max_cl;
+            const int pairs = p.n_items / 2;
+            const int n_cl = pairs < max_cl ? pairs : max_cl;
             cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(2 * clusters);
+            cfg.gridDim = dim3(2 * n_cl);
             cfg.blockDim = dim3(NUM_THREADS);
             cfg.dynamicSmemBytes = C::SMEM;
             cfg.stream = st;
@@ -568,13 +594,55 @@ cudaError_t launch_d(const TcLaunch &a, cudaStream_t st)
             at[0].val.clusterDim.z = 1;
             cfg.attrs = at;
             cfg.numAttrs = 1;
-            e = cudaLaunchKernelEx(&cfg, ra_attn_tc_kernel<D, 2>, p);
+            e = cudaLaunchKernelEx(&cfg, ra_attn_tc_kernel<D, 2, SPLIT>, p);
             return e != cudaSuccess ? e : cudaGetLastError();
         }
     }
-    const int grid = p.n_units < a.sm_count ? p.n_units : a.sm_count;
-    ra_attn_tc_kernel<D, 1><<<grid, NUM_THREADS, C::SMEM, st>>>(p);
+    if ((e = set_smem_attr<D, 1, SPLIT>()) != cudaSuccess)
+        return e;
+    const int grid = p.n_items < sm_count ? p.n_items : sm_count;
+    ra_attn_tc_kernel<D, 1, SPLIT><<<grid, NUM_THREADS, C::SMEM, st>>>(p);
     return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const TcLaunch &a, cudaStream_t st)
+{
+    TcParams p;
+    memset(&p, 0, sizeof(p));
+    if (!encode_rows(&p.tm_q, a.q, (long long)a.B * a.H * a.S, D) ||
+        !encode_rows(&p.tm_k, a.k, (long long)a.B * a.Hkv * a.S, D) ||
+        !encode_rows(&p.tm_v, a.v, (long long)a.B * a.Hkv * a.S, D))
+        return cudaErrorInvalidValue;
+    p.sp = ra_unit_space_ranks(ra_unit_space(a.B, a.H, a.Hkv, a.S, a.N, a.layout, a.causal, a.s_begin, a.s_end),
+                               a.rank_lo, a.rank_hi);
+    const long long n_units = ra_unit_count(p.sp);
+    const int nsplit = a.nsplit > 1 ? a.nsplit : 1;
+    if (n_units * nsplit > 0x7fffffffll || (nsplit > 1 && !a.out_f32))
+        return cudaErrorInvalidValue;
+    p.out = a.out;
+    p.lse = a.lse;
+    p.n_items = (int)(n_units * nsplit);
+    p.nsplit = nsplit;
+    p.pair_items = n_units % 2 == 0 ? 1 : 0;
+    p.split_out_bytes = nsplit > 1 ? a.split_out_bytes : 0;
+    p.split_lse_stride = nsplit > 1 ? a.split_lse_stride : 0;
+    p.H = a.H, p.Hkv = a.Hkv, p.S = a.S, p.N = a.N, p.L = a.S / a.N;
+    p.layout = a.layout, p.causal = a.causal;
+    p.s_begin = a.s_begin, p.s_end = a.s_end, p.out_f32 = a.out_f32;
+    p.ntiles = (p.L + RA_TILE - 1) / RA_TILE;
+    p.scale_log2 = 1.4426950408889634f / sqrtf((float)D);
+    p.timeout_ns = a.timeout_ns;
+    if (p.n_items <= 0)
+        return cudaSuccess;
+    // Clusters need units (2m, 2m + 1) with one key/value walk: two head
+    // pairs of one kv head next to each other in the order, i.e. an even
+    // number of head pairs per kv head (the pieces of a split walk keep the
+    // two units' pieces k next to each other).
+    const int pairs_per_kv = p.sp.head_pairs ? (a.H / a.Hkv) / 2 : 0;
+    const bool clusters = a.cluster == 2 && pairs_per_kv >= 2 && pairs_per_kv % 2 == 0 && n_units % 2 == 0;
+    return nsplit > 1 ? launch_grid<D, true>(p, clusters, a.sm_count, st)
+                      : launch_grid<D, false>(p, clusters, a.sm_count, st);
 }
 
 }  // namespace

@@ -81,7 +81,19 @@ struct TcLaunch {
     unsigned long long timeout_ns;
     int sm_count;
     int cluster;                 // 2: share K/V loads between CTA pairs where the units allow
+    // > 1: cut every unit's walk over its key tiles into nsplit pieces, each
+    // a work item writing its own normalised fp32 partial (out_f32 = 1) at
+    // out + k split_out_bytes and lse + k split_lse_stride (k = piece)
+    int nsplit;
+    long long split_out_bytes, split_lse_stride;
 };
+
+// Folds nsplit normalised fp32 partials per row (kernel order; partial k of
+// row r at part[(k part_stride + r) d], lse at part_lse[k part_stride + r])
+// into the output in natural order (bf16 or fp32) and its lse.
+void launch_combine(const float *part, const float *part_lse, int nsplit, long long part_stride, void *out,
+                    float *lse, int out_bf16, long long rows_total, int S, int N, int striped, int d,
+                    int sm_count, cudaStream_t st);
 
 // Backward pass (bf16, d in {64, 128}): delta = rowsum(dout * out), then the
 // dK/dV and dQ tensor-core kernels.  All tensors in the layout's rank-major

@@ -5,6 +5,7 @@
 //   * ra_all_to_all_kernel sequence-sharded <-> head-sharded relayout (Ulysses)
 //   * ra_merge_kernel     running-softmax merge of one ring step's partials
 //   * ra_finalize_kernel  fp32 running result -> output dtype, natural order
+//   * ra_combine_kernel   the pieces of a split ring walk -> output, natural order
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -560,6 +561,85 @@ void launch_finalize(const float *run, const float *run_lse, void *out, float *l
     else
         ra_finalize_kernel<float><<<(int)blocks, threads, 0, st>>>(
             run, run_lse, (float *)out, lse, rows_total, S, L, N, striped, d);
+}
+
+// ---------------------------------------------------------------- combine
+// The nsplit normalised fp32 partials (out_k, lse_k) of every query row
+// (kernel order, partial k at part + k part_stride rows) folded into the
+// final row: lse = log sum_k exp(lse_k), out = sum_k exp(lse_k - lse) out_k,
+// written in natural order (striped rows scattered back to t(p)); bf16
+// output is rounded to nearest even.  A partial with lse_k = -inf holds no
+// key and is not read.  The same running-softmax merge as ra_merge_kernel,
+// over nsplit partials at once.
+template <typename OUT>
+__global__ void ra_combine_kernel(const float *__restrict__ part, const float *__restrict__ part_lse, int nsplit,
+                                  long long part_stride, OUT *__restrict__ out, float *__restrict__ lse,
+                                  long long rows_total, int S, int L, int N, int striped, int d)
+{
+    const int vpr = d / 4;  // 16-byte vectors per row
+    const long long n = rows_total * vpr;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const long long row = idx / vpr;
+        const int c4 = (int)(idx - row * vpr);
+        float m = -INFINITY;
+        for (int k = 0; k < nsplit; ++k)
+            m = fmaxf(m, part_lse[k * part_stride + row]);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float sum = 0.f;
+        if (m != -INFINITY) {
+            for (int k = 0; k < nsplit; ++k) {
+                const float lk = part_lse[k * part_stride + row];
+                if (lk == -INFINITY)
+                    continue;
+                const float wk = expf(lk - m);
+                const float4 x = reinterpret_cast<const float4 *>(part + (k * part_stride + row) * d)[c4];
+                acc.x += wk * x.x;
+                acc.y += wk * x.y;
+                acc.z += wk * x.z;
+                acc.w += wk * x.w;
+                sum += wk;
+            }
+            const float inv = 1.f / sum;
+            acc.x *= inv, acc.y *= inv, acc.z *= inv, acc.w *= inv;
+        }
+        const long long bh = row / S;
+        const int p = (int)(row - bh * S);
+        const int t = striped ? (p % L) * N + p / L : p;
+        const long long drow = bh * S + t;
+        if constexpr (sizeof(OUT) == 4) {
+            reinterpret_cast<float4 *>(out + drow * d)[c4] = acc;
+        } else {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+            uint2 w;
+            w.x = *reinterpret_cast<uint32_t *>(&lo);
+            w.y = *reinterpret_cast<uint32_t *>(&hi);
+            reinterpret_cast<uint2 *>(out + drow * d)[c4] = w;
+        }
+        if (c4 == 0)
+            lse[drow] = m == -INFINITY ? -INFINITY : m + logf(sum);
+    }
+}
+
+void launch_combine(const float *part, const float *part_lse, int nsplit, long long part_stride, void *out,
+                    float *lse, int out_bf16, long long rows_total, int S, int N, int striped, int d,
+                    int sm_count, cudaStream_t st)
+{
+    const int threads = 256;
+    long long blocks = (rows_total * (d / 4) + threads - 1) / threads;
+    const long long cap = (long long)sm_count * 8;
+    if (blocks > cap)
+        blocks = cap;
+    if (blocks < 1)
+        blocks = 1;
+    const int L = S / N;
+    if (out_bf16)
+        ra_combine_kernel<__nv_bfloat16><<<(int)blocks, threads, 0, st>>>(
+            part, part_lse, nsplit, part_stride, (__nv_bfloat16 *)out, lse, rows_total, S, L, N, striped, d);
+    else
+        ra_combine_kernel<float><<<(int)blocks, threads, 0, st>>>(
+            part, part_lse, nsplit, part_stride, (float *)out, lse, rows_total, S, L, N, striped, d);
 }
 
 }  // namespace ra

@@ -38,8 +38,9 @@
  *     stay valid until the enqueued work has finished.  `out` and `lse` must
  *     not overlap any input.
  *   - Every buffer (inputs, outputs, caller workspace) must be device memory
- *     of the CURRENT device: each call checks the first and last byte of each
- *     one with cudaPointerGetAttributes and returns RA_ERR_INVALID_ARG
+ *     of the CURRENT device: each call checks each one (the allocation its
+ *     first byte lies in) with cudaPointerGetAttributes and returns
+ *     RA_ERR_INVALID_ARG
  *     (RA_ERR_WORKSPACE for a workspace) for pinned or pageable host memory,
  *     managed memory, or another GPU's memory reached through unified
  *     addressing, before anything is enqueued.  The attention kernels load
@@ -110,6 +111,13 @@ typedef enum { RA_DTYPE_BF16 = 0, RA_DTYPE_F32 = 1 } ra_dtype;
  * bf16 operands on the tensor cores; out is rounded to bf16 (nearest even).
  * Supported: d in {64, 128}; any block length L >= 1.  Uses RA_MODE_FUSED and
  * allocates its scratch stream-ordered (cudaMallocAsync on `stream`).
+ * Small problems, whose work units (pairs of 128-row query tiles) cannot
+ * fill half the current device's SMs, have every unit's walk over its key
+ * tiles (in ring order) cut into up to SMs / units pieces (at most 16)
+ * computed by different CTAs as independent fp32 partials, which a second
+ * kernel folds by the running-softmax merge into out and lse (the ring's own
+ * decomposition: each block's partial result is merged into the running one,
+ * "Ring Attention" page, section "Halka Dikkati Nasil Calisir").
  * Returns RA_ERR_INVALID_ARG for B, H, Hkv, S, n_blocks < 1, H % Hkv != 0,
  * S % n_blocks != 0, layout not in ra_layout, null, misaligned or overlapping
  * pointers; RA_ERR_UNSUPPORTED for other d.
@@ -132,8 +140,11 @@ ra_status ra_forward_f32(const float *q, const float *k, const float *v, float *
 /*
  * ra_workspace_bytes - bytes of scratch ra_forward_ws needs for this problem
  * (striped copies of q, k, v, out and lse; per-step running and partial
- * results; for RA_MODE_RING two rotating copies of k and v).  0 when none is
- * needed (bf16 contiguous fused).
+ * results; for RA_MODE_RING two rotating copies of k and v; for small bf16
+ * fused problems whose walks are split (see ra_forward), the pieces' fp32
+ * partials of out and lse).  0 when none is needed (bf16 contiguous fused
+ * without a split).  The split depends on the SM count of the CURRENT
+ * device, so ask with the device current that ra_forward_ws will run on.
  * dtype is a ra_dtype, mode a ra_mode.  Returns 0 for an invalid request.
  */
 size_t ra_workspace_bytes(int B, int H, int Hkv, int S, int d, int n_blocks, int layout,
@@ -307,8 +318,11 @@ ra_status ra_backward_ws(const void *q, const void *k, const void *v, const void
  * synchronisation or an out-of-memory failure half way through.  ra_forward
  * gets its striped scratch with cudaMallocAsync; this entry point does not.
  *
- * Its scratch (for RA_LAYOUT_STRIPED, the striped copies of q, k, v, out and
- * lse: 2 (B H + 2 B Hkv) S d + 4 B H S bytes; contiguous problems need none)
+ * Its scratch is exactly the workspace ra_forward would allocate
+ * (ra_workspace_bytes with RA_MODE_FUSED: for RA_LAYOUT_STRIPED the striped
+ * copies of q, k, v, out and lse, 2 (B H + 2 B Hkv) S d + 4 B H S bytes; for
+ * small problems whose walks are split, the pieces' fp32 partials; large
+ * contiguous problems need none).  It
  * lives in one fixed array of RA_NOALLOC_SCRATCH_BYTES (64 MiB) that is part
  * of the library's device image: every GPU that loads the library holds it
  * until the process exits.  A problem whose scratch would not fit returns
