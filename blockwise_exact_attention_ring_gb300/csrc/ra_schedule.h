@@ -121,10 +121,11 @@ struct RaUnitSpace {
 };
 
 // Key/value rows (B * Hkv * S) from which the dealing order groups work by kv
-// head: below this the K and V of all heads stay in L2 and a global
-// heaviest-first order balances the tail better; above it (e.g. 256K tokens
-// x 8 kv heads = 1 GB of K and V) grouping by head keeps L2 reuse.
-#define RA_KV_OUTER_ROWS (1ll << 20)
+// head: below this the K and V of all heads stay in L2 (32K tokens x 8 kv
+// heads x d = 128: 134 MB against a 126 MB L2) and a global heaviest-first
+// order balances the tail better; from it on (64K tokens x 8 kv heads: 268 MB
+// of K and V, 1 GB at 256K) grouping by head keeps L2 reuse.
+#define RA_KV_OUTER_ROWS (1ll << 19)
 
 RA_HD RaUnitSpace ra_unit_space(int B, int H, int Hkv, int S, int n_blocks, int layout, int causal,
                                 int s_begin, int s_end)

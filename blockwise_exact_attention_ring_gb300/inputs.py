@@ -67,6 +67,13 @@ WORKLOADS: Dict[str, Workload] = {w.name: w for w in [
     Workload("ring32-s1m-h32kv8-d128-causal-striped", 1, 32, 8, 1048576, 128, 32,
              LAYOUT_STRIPED, True, "bf16", 1005, std=0.5, spike_frac=0.01,
              spike_scale=8.0),
+    # profiling proxies of the 256K shape (memory-counter captures stay a few
+    # GB on the device): the same heads and ranks at 64K and 128K tokens, whose
+    # K and V (268 MB, 537 MB) already exceed the 126 MB L2
+    Workload("ring8-s64k-h32kv8-d128-causal-striped", 1, 32, 8, 65536, 128, 8,
+             LAYOUT_STRIPED, True, "bf16", 1006),
+    Workload("ring8-s128k-h32kv8-d128-causal-striped", 1, 32, 8, 131072, 128, 8,
+             LAYOUT_STRIPED, True, "bf16", 1007),
 ]}
 
 

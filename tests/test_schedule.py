@@ -115,7 +115,7 @@ def test_kernel_units_cover_every_tile_once_heaviest_first(B, H, Hkv, S, N, layo
     assert set(seen) == set(active)
     for k, c in seen.items():
         assert c >= active[k]
-    _check_order(units, H, Hkv, B * Hkv * S >= (1 << 20))
+    _check_order(units, H, Hkv, B * Hkv * S >= (1 << 19))
 
 
 def _check_order(units, H, Hkv, kv_outer):
