@@ -31,8 +31,8 @@ def _call(fn, q, k, v, out, lse, N, layout, causal):
 
 @pytest.mark.parametrize("variant", [0, 1], ids=["clusters", "one-cta"])
 @pytest.mark.parametrize("B,H,Hkv,S,d,N,layout,causal", [
-    (1, 8, 2, 2048, 128, 4, 1, True),    # striped: striped copies in the array; CTA clusters apply
-    (1, 4, 2, 1000, 128, 2, 0, True),    # contiguous, ragged block: no scratch used
+    (1, 8, 2, 2048, 128, 4, 1, True),    # striped: striped copies and split-walk partials; CTA clusters
+    (1, 4, 2, 1000, 128, 2, 0, True),    # contiguous, ragged block: split-walk partials only
     (2, 2, 2, 1536, 64, 3, 1, False),    # d = 64, tile pairs, non-causal striped
 ])
 def test_noalloc_matches_ra_forward_twice(B, H, Hkv, S, d, N, layout, causal, variant):
@@ -56,6 +56,22 @@ def test_noalloc_matches_ra_forward_twice(B, H, Hkv, S, d, N, layout, causal, va
     ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=causal)
     assert np.abs(out.float().cpu().numpy() - ro).max() < 2e-2
     assert np.abs(lse.cpu().numpy() - rl).max() < 1e-3
+
+
+def test_noalloc_runs_a_large_contiguous_problem_without_scratch():
+    """A contiguous problem large enough to fill the GPU needs no scratch at
+    all (no striped copies, no split walks): it runs with the array untouched
+    and equals ra_forward bit for bit."""
+    B, H, Hkv, S, d, N = 1, 16, 4, 8192, 128, 4
+    assert ra.workspace_bytes(B, H, Hkv, S, d, N, "contiguous", True, "fused") == 0
+    L = ra.lib()
+    q, k, v = (t.cuda() for t in inputs.make_qkv(B, H, Hkv, S, d, seed=12))
+    ref_o, ref_l = ra.forward(q, k, v, n_blocks=N, causal=True)
+    out = torch.empty_like(q)
+    lse = torch.empty(B, H, S, device="cuda", dtype=torch.float32)
+    assert _call(L.ra_forward_noalloc, q, k, v, out, lse, N, 0, True) == rb.RA_OK
+    ra.check()
+    assert torch.equal(out, ref_o) and torch.equal(lse, ref_l)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
