@@ -50,9 +50,11 @@ def test_short_wait_limit_does_not_trip_a_healthy_run():
     L.ra_set_wait_timeout_ns(100_000_000)
     try:
         # group 2 runs one CTA per unit; group 4 runs CTA pairs whose waits
-        # include the peer's multicast copies and stage releases
-        for H, Hkv in ((4, 2), (8, 2)):
-            q, k, v = (t.cuda() for t in inputs.make_qkv(1, H, Hkv, 4096, 128, seed=78))
+        # include the peer's multicast copies and stage releases; the short
+        # sequences split every unit's walk into pieces (empty pieces skip
+        # every wait)
+        for H, Hkv, S in ((4, 2, 4096), (8, 2, 4096), (4, 2, 1024), (8, 2, 512)):
+            q, k, v = (t.cuda() for t in inputs.make_qkv(1, H, Hkv, S, 128, seed=78))
             ra.forward(q, k, v, n_blocks=4, causal=True)
             ra.check()
     finally:
