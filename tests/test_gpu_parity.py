@@ -253,3 +253,21 @@ def test_check_reports_ok_after_clean_runs():
     q, k, v = _dev(*inputs.make_qkv(1, 2, 1, 256, 64, seed=1))
     ra.forward(q, k, v, n_blocks=2, causal=True)
     ra.check()   # raises on a device-side timeout
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+@pytest.mark.parametrize("spikes", [False, True])
+def test_bf16_d64_long_walks(layout, spikes):
+    """Head dimension 64 rotates three S/P buffers between the two query
+    tiles of a CTA (the S product of a tile's next key tile is issued before
+    that tile's P V).  A problem large enough for many units per CTA and long
+    ring walks (no split), causal, against the oracle on 1024 sampled rows;
+    with spikes, 5 % of the keys scaled by 16 move the running max often."""
+    B, H, Hkv, S, d, N = 1, 16, 4, 16384, 64, 4
+    kw = dict(spike_frac=0.05, spike_scale=16.0) if spikes else {}
+    q, k, v = _dev(*inputs.make_qkv(B, H, Hkv, S, d, seed=640 + spikes, **kw))
+    assert ra.workspace_bytes(B, H, Hkv, S, d, N, "contiguous", True, "fused") == 0  # no split
+    out, lse = ra.forward(q, k, v, n_blocks=N, layout=layout, causal=True)
+    ra.check()
+    rows = inputs.sample_rows(B, H, S, N, n=1024, seed=11).numpy()
+    _check(out, lse, q, k, v, True, rows=rows)
