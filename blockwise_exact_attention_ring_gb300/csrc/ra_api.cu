@@ -858,14 +858,14 @@ long long ra_backward_tile_pairs(int B, int H, int Hkv, int S, int n_blocks, int
         long long k = 0;
         if (which == 0) {
             int bhkv, j, tb;
-            ra_bwd_dkdv_unit((int)u, B, Hkv, n_blocks, ntiles, layout, bhkv, j, tb);
+            ra_bwd_dkdv_unit((int)u, B, Hkv, n_blocks, ntiles, layout, ra_bwd_kv_outer(B, Hkv, S), bhkv, j, tb);
             const int b = bhkv / Hkv, g = bhkv % Hkv;
             RaQWalk w;
             for (w.start(j, tb, n_blocks, layout, causal, ntiles, grp); w.valid(); w.advance())
                 put(u, b * H + g * grp + w.hh, w.i, w.ta, j, tb, k++);
         } else {
             int bh, i, ta;
-            ra_bwd_dq_unit((int)u, B, H, n_blocks, ntiles, layout, bh, i, ta);
+            ra_bwd_dq_unit((int)u, B, H, Hkv, n_blocks, ntiles, layout, ra_bwd_kv_outer(B, Hkv, S), bh, i, ta);
             RaKWalk w;
             for (w.start(i, ta, n_blocks, layout, causal, ntiles); w.valid(); w.advance())
                 put(u, bh, i, ta, w.j, w.tb, k++);

@@ -83,12 +83,23 @@ struct RaKWalk {
 // Unit u of the dK/dV kernel -> (batch * Hkv + kv head, block j, key tile tb),
 // heaviest first: contiguous causal blocks are seen by every later block, so
 // ascending (j, tb); otherwise tb ascending outermost (early key tiles of a
-// block meet more query tiles on diagonal blocks).
-RA_HD void ra_bwd_dkdv_unit(int u, int B, int Hkv, int N, int ntiles, int layout, int &bhkv, int &j, int &tb)
+// block meet more query tiles on diagonal blocks).  With kv_outer (the K/V of
+// all heads far exceed L2, as in the forward's dealing order) the kv head is
+// the outermost index, so the units in flight stream one kv group's Q and dO
+// together; otherwise it is the fastest one.
+RA_HD void ra_bwd_dkdv_unit(int u, int B, int Hkv, int N, int ntiles, int layout, int kv_outer, int &bhkv, int &j,
+                            int &tb)
 {
     const int nkv = B * Hkv;
-    bhkv = u % nkv;
-    const int r = u / nkv;
+    int r;
+    if (kv_outer) {
+        const int per_kv = N * ntiles;
+        bhkv = u / per_kv;
+        r = u - bhkv * per_kv;
+    } else {
+        bhkv = u % nkv;
+        r = u / nkv;
+    }
     if (layout == 0) {
         j = r / ntiles, tb = r % ntiles;
     } else {
@@ -97,16 +108,38 @@ RA_HD void ra_bwd_dkdv_unit(int u, int B, int Hkv, int N, int ntiles, int layout
 }
 
 // Unit u of the dQ kernel -> (batch * H + head, block i, query tile ta),
-// latest in the causal order (heaviest) first.
-RA_HD void ra_bwd_dq_unit(int u, int B, int H, int N, int ntiles, int layout, int &bh, int &i, int &ta)
+// latest in the causal order (heaviest) first.  With kv_outer the kv group is
+// the outermost index and its query heads the fastest, so the units in flight
+// walk one kv head's K and V together; otherwise the head is the fastest
+// index over all heads.
+RA_HD void ra_bwd_dq_unit(int u, int B, int H, int Hkv, int N, int ntiles, int layout, int kv_outer, int &bh, int &i,
+                          int &ta)
 {
     const int nq = B * H;
-    bh = u % nq;
-    const int r = u / nq;
+    int r;
+    if (kv_outer) {
+        const int grp = H / Hkv;
+        const int per_kv = grp * N * ntiles;
+        const int kvi = u / per_kv;                   // batch * Hkv + kv head
+        const int rem = u - kvi * per_kv;
+        const int b = kvi / Hkv;
+        bh = b * H + (kvi - b * Hkv) * grp + rem % grp;
+        r = rem / grp;
+    } else {
+        bh = u % nq;
+        r = u / nq;
+    }
     if (layout == 0) {
         const int q = N * ntiles - 1 - r;
         i = q / ntiles, ta = q % ntiles;
     } else {
         ta = ntiles - 1 - r / N, i = N - 1 - r % N;
     }
+}
+
+// Whether the backward kernels deal their units by kv head (the forward's
+// rule: B * Hkv * S key/value rows at or above RA_KV_OUTER_ROWS).
+RA_HD int ra_bwd_kv_outer(int B, int Hkv, int S)
+{
+    return (long long)B * Hkv * S >= RA_KV_OUTER_ROWS ? 1 : 0;
 }

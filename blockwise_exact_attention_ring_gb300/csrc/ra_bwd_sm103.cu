@@ -254,7 +254,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dkdv_kernel(const __gri
     auto bar = [&](uint64_t &b) { return smem_u32(&b); };
 
     int bhkv, j, tb;
-    ra_bwd_dkdv_unit(blockIdx.x, p.B, p.Hkv, p.N, p.ntiles, p.layout, bhkv, j, tb);
+    ra_bwd_dkdv_unit(blockIdx.x, p.B, p.Hkv, p.N, p.ntiles, p.layout, ra_bwd_kv_outer(p.B, p.Hkv, p.S), bhkv, j,
+                     tb);
     const int b = bhkv / p.Hkv, g = bhkv % p.Hkv, grp = p.H / p.Hkv;
     const int kvrow = bhkv * p.S + j * p.L + tb * RA_TILE;
 
@@ -512,7 +513,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dq_kernel(const __grid_
     auto bar = [&](uint64_t &b) { return smem_u32(&b); };
 
     int bh, i, ta;
-    ra_bwd_dq_unit(blockIdx.x, p.B, p.H, p.N, p.ntiles, p.layout, bh, i, ta);
+    ra_bwd_dq_unit(blockIdx.x, p.B, p.H, p.Hkv, p.N, p.ntiles, p.layout, ra_bwd_kv_outer(p.B, p.Hkv, p.S), bh, i,
+                   ta);
     const int b = bh / p.H, h = bh % p.H;
     const int kvbh = b * p.Hkv + h / (p.H / p.Hkv);
     const int qrow = bh * p.S + i * p.L + ta * RA_TILE;

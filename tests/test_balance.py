@@ -106,7 +106,8 @@ def _visible_tile_pairs(B, H, S, N, layout, causal):
     return out
 
 
-@pytest.mark.parametrize("B,H,Hkv,S,N", [(1, 4, 2, 1024, 4), (2, 3, 1, 768, 3), (1, 2, 2, 640, 5)])
+@pytest.mark.parametrize("B,H,Hkv,S,N", [(1, 4, 2, 1024, 4), (2, 3, 1, 768, 3), (1, 2, 2, 640, 5),
+                                         (8, 128, 64, 1024, 4)])  # 2^19 K/V rows: units grouped by kv head
 @pytest.mark.parametrize("layout,causal", [("contiguous", True), ("striped", True), ("contiguous", False)])
 def test_backward_kernels_cover_every_visible_tile_pair_once(B, H, Hkv, S, N, layout, causal):
     """Both backward kernels visit exactly the tile pairs with a visible key,
@@ -168,3 +169,20 @@ def test_cluster_pairs_within_one_devices_step(layout, causal):
             a, b = u[0::2], u[1::2]
             assert np.array_equal(kv(a[:, 0]), kv(b[:, 0]))
             assert np.array_equal(a[:, [1, 3, 4, 5, 6]], b[:, [1, 3, 4, 5, 6]])
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+def test_backward_units_grouped_by_kv_head_on_large_problems(layout):
+    """From 2^19 key/value rows the backward kernels deal their units kv head
+    by kv head (the units in flight then stream one kv group's data), as the
+    forward does; below it the head index runs fastest."""
+    B, H, Hkv, S, N = 8, 128, 64, 1024, 4           # B * Hkv * S = 2^19
+    grp = H // Hkv
+    for which in (0, 1):
+        pairs = ra.backward_tile_pairs(B, H, Hkv, S, N, layout, True, which)
+        units = pairs[np.unique(pairs[:, 0], return_index=True)[1]]
+        kv = units[:, 1] // H * Hkv + units[:, 1] % H // grp
+        assert np.all(np.diff(kv) >= 0), which      # kv head outermost, non-decreasing
+    small = ra.backward_tile_pairs(1, 4, 2, 1024, 4, layout, True, 1)
+    units = small[np.unique(small[:, 0], return_index=True)[1]]
+    assert list(units[:4, 1]) == [0, 1, 2, 3]       # head fastest below the threshold
