@@ -80,7 +80,7 @@ struct Cfg {
 struct Ctrl {
     uint64_t q_full, q_empty;
     uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-    uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
+    uint64_t s_full[2], p_full[2], o_done[2], o_free[2];  // o_done: once per unit, after its last P V
     uint64_t final_bar;
     uint32_t tmem_base;
     int abort;
@@ -377,7 +377,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
                         break;
                     tc_fence_after();
                     issue_pv(0, vs, jj > 0);
-                    mma_commit(bar(ctrl->o_done[0]));
+                    if (!more)
+                        mma_commit(bar(ctrl->o_done[0]));  // O of tile 0 complete for the unit
                     if (more) {
                         ks = kcnt % C::KSTAGES;
                         if (!(ok = kv_wait(bar(ctrl->k_full[ks]), (kcnt / C::KSTAGES) & 1, SITE_K_FULL)))
@@ -393,7 +394,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
                         break;
                     tc_fence_after();
                     issue_pv(1, vs, jj > 0);
-                    mma_commit(bar(ctrl->o_done[1]));
+                    if (!more)
+                        mma_commit(bar(ctrl->o_done[1]));  // O of tile 1 complete for the unit
                     kv_release(bar(ctrl->v_empty[vs]));
                     ++vcnt;
                     if (more) {
@@ -445,14 +447,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
             if (SPLIT)
                 w.skip(t0);
             for (int jj = 0; SPLIT ? jj < cnt : w.valid(); w.advance(), ++jj) {
+                // S(t, jj) was issued after P V(t, jj - 1), and the commit that
+                // signals S tracks every earlier MMA of the issuing thread: once
+                // S is here, the previous P V has read P and written O, so P may
+                // be overwritten and O rescaled without a wait of its own
                 if (!(ok = wait_warp(bar(ctrl->s_full[t]), scnt & 1, abort, tmo, SITE_S_FULL)))
                     break;
                 ++scnt;
-                if (jj > 0) {
-                    if (!(ok = wait_warp(bar(ctrl->o_done[t]), ocnt & 1, abort, tmo, SITE_O_DONE)))
-                        break;
-                    ++ocnt;
-                }
                 tc_fence_after();
                 const int lim = ra_key_limit(w.cls, a, p.L) - w.tb * RA_TILE;
                 // masked only where some column of the warp's rows lies past
