@@ -318,102 +318,129 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0);
-            constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, 1);
-            auto issue_s = [&](int t, int ks) {
-                const uint32_t qa = sQ + t * C::TILE, ka = sK + ks * C::TILE;
+        // The whole warp runs the loop on warp-uniform values, waits included,
+        // and one lane, elected once, issues every MMA and commit (a commit
+        // tracks the MMAs of the thread that executes it).  A tcgen05.mma issue
+        // returns only once the tensor pipe takes it, about one MMA ahead, so
+        // whatever the issuing thread does between MMAs leaves the pipe idle; a
+        // barrier wait costs far less in converged, uniform code than inside a
+        // one-lane branch.
+        const bool leader = elect_one();
+        const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
+        constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0);
+        constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, 1);
+        auto issue_s = [&](int t, int ks) {
+            const uint32_t qa = sQ + t * C::TILE, ka = sK + ks * C::TILE;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::SLAB + (kk & 3) * 32;
-                    mma_ss(tmem + t * 128, smem_desc_sw128(qa + off, 16, 1024),
-                           smem_desc_sw128(ka + off, 16, 1024), IDESC_S, kk > 0);
-                }
-            };
-            auto issue_pv = [&](int t, int vs, bool acc) {
-                const uint32_t va = sV + vs * C::TILE;
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * C::SLAB + (kk & 3) * 32;
+                mma_ss(tm + t * 128, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
+                       IDESC_S, kk > 0);
+            }
+        };
+        auto issue_pv = [&](int t, int vs, bool acc) {
+            const uint32_t va = sV + vs * C::TILE;
 #pragma unroll
-                for (int kk = 0; kk < RA_TILE / 16; ++kk)
-                    mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
-                           smem_desc_sw128(va + kk * 2048, C::SLAB, 1024), IDESC_PV,
-                           (acc || kk > 0) ? 1u : 0u);
-            };
-            uint32_t kcnt = 0, vcnt = 0, qcnt = 0, pcnt = 0;
-            bool ok = true;
-            for (int r = 0; ok; ++r) {
-                const int wi = unit_of(r);
-                if (wi >= p.n_items)
-                    break;
-                int k = 0, t0 = 0, n = 0;
-                if (SPLIT)
-                    item_decode(p, wi, k, t0, n);
-                else
-                    n = ra_unit_decode(p.sp, wi).cost;
-                if (SPLIT && n == 0)
-                    continue;  // an empty piece: no MMA
-                if (!(ok = wait1(bar(ctrl->q_full), qcnt & 1, abort, tmo, SITE_Q_FULL)))
-                    break;
-                int ks = kcnt % C::KSTAGES;
-                if (!(ok = kv_wait(bar(ctrl->k_full[ks]), (kcnt / C::KSTAGES) & 1, SITE_K_FULL)))
-                    break;
-                tc_fence_after();
+            for (int kk = 0; kk < RA_TILE / 16; ++kk)
+                mma_ts(tm + 256 + t * 128, tm + t * 128 + kk * 8, smem_desc_sw128(va + kk * 2048, C::SLAB, 1024),
+                       IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+        };
+        auto wwait = [&](uint32_t b, uint32_t parity, unsigned int site) {
+            return wait_warp(b, parity, abort, tmo, site);
+        };
+        auto kv_wwait = [&](uint32_t b, uint32_t parity, unsigned int site) -> bool {
+            if (CL == 2)
+                return __all_sync(0xffffffffu, wait1c(b, parity, abort, tmo, site)) != 0;
+            return wait_warp(b, parity, abort, tmo, site);
+        };
+        uint32_t kcnt = 0, vcnt = 0, qcnt = 0, pcnt = 0;
+        bool ok = true;
+        for (int r = 0; ok; ++r) {
+            const int wi = unit_of(r);
+            if (wi >= p.n_items)
+                break;
+            int k = 0, t0 = 0, n = 0;
+            if (SPLIT)
+                item_decode(p, wi, k, t0, n);
+            else
+                n = ra_unit_decode(p.sp, wi).cost;
+            if (SPLIT && n == 0)
+                continue;  // an empty piece: no MMA
+            if (!(ok = wwait(bar(ctrl->q_full), qcnt & 1, SITE_Q_FULL)))
+                break;
+            int ks = kcnt % C::KSTAGES;
+            if (!(ok = kv_wwait(bar(ctrl->k_full[ks]), (kcnt / C::KSTAGES) & 1, SITE_K_FULL)))
+                break;
+            tc_fence_after();
+            if (leader) {
                 issue_s(0, ks);
                 mma_commit(bar(ctrl->s_full[0]));
                 issue_s(1, ks);
                 mma_commit(bar(ctrl->s_full[1]));
                 kv_release(bar(ctrl->k_empty[ks]));
-                ++kcnt;
                 if (n == 1)
                     mma_commit(bar(ctrl->q_empty));
-                for (int jj = 0; jj < n; ++jj) {
-                    const int vs = vcnt % C::VSTAGES;
-                    const bool more = jj + 1 < n;
-                    if (!(ok = kv_wait(bar(ctrl->v_full[vs]), (vcnt / C::VSTAGES) & 1, SITE_V_FULL)))
-                        break;
-                    if (jj == 0 && qcnt > 0 &&
-                        !(ok = wait1(bar(ctrl->o_free[0]), (qcnt - 1) & 1, abort, tmo, SITE_O_FREE)))
-                        break;
-                    if (!(ok = wait1(bar(ctrl->p_full[0]), pcnt & 1, abort, tmo, SITE_P_FULL)))
-                        break;
-                    tc_fence_after();
+            }
+            __syncwarp();
+            ++kcnt;
+            for (int jj = 0; jj < n; ++jj) {
+                const int vs = vcnt % C::VSTAGES;
+                const bool more = jj + 1 < n;
+                if (!(ok = kv_wwait(bar(ctrl->v_full[vs]), (vcnt / C::VSTAGES) & 1, SITE_V_FULL)))
+                    break;
+                if (jj == 0 && qcnt > 0 && !(ok = wwait(bar(ctrl->o_free[0]), (qcnt - 1) & 1, SITE_O_FREE)))
+                    break;
+                if (!(ok = wwait(bar(ctrl->p_full[0]), pcnt & 1, SITE_P_FULL)))
+                    break;
+                tc_fence_after();
+                if (leader) {
                     issue_pv(0, vs, jj > 0);
                     if (!more)
                         mma_commit(bar(ctrl->o_done[0]));  // O of tile 0 complete for the unit
-                    if (more) {
-                        ks = kcnt % C::KSTAGES;
-                        if (!(ok = kv_wait(bar(ctrl->k_full[ks]), (kcnt / C::KSTAGES) & 1, SITE_K_FULL)))
-                            break;
-                        tc_fence_after();
+                }
+                __syncwarp();
+                if (more) {
+                    ks = kcnt % C::KSTAGES;
+                    if (!(ok = kv_wwait(bar(ctrl->k_full[ks]), (kcnt / C::KSTAGES) & 1, SITE_K_FULL)))
+                        break;
+                    tc_fence_after();
+                    if (leader) {
                         issue_s(0, ks);
                         mma_commit(bar(ctrl->s_full[0]));
                     }
-                    if (jj == 0 && qcnt > 0 &&
-                        !(ok = wait1(bar(ctrl->o_free[1]), (qcnt - 1) & 1, abort, tmo, SITE_O_FREE)))
-                        break;
-                    if (!(ok = wait1(bar(ctrl->p_full[1]), pcnt & 1, abort, tmo, SITE_P_FULL)))
-                        break;
-                    tc_fence_after();
+                    __syncwarp();
+                }
+                if (jj == 0 && qcnt > 0 && !(ok = wwait(bar(ctrl->o_free[1]), (qcnt - 1) & 1, SITE_O_FREE)))
+                    break;
+                if (!(ok = wwait(bar(ctrl->p_full[1]), pcnt & 1, SITE_P_FULL)))
+                    break;
+                tc_fence_after();
+                if (leader) {
                     issue_pv(1, vs, jj > 0);
                     if (!more)
                         mma_commit(bar(ctrl->o_done[1]));  // O of tile 1 complete for the unit
                     kv_release(bar(ctrl->v_empty[vs]));
-                    ++vcnt;
                     if (more) {
                         issue_s(1, ks);
                         mma_commit(bar(ctrl->s_full[1]));
                         kv_release(bar(ctrl->k_empty[ks]));
-                        ++kcnt;
                         if (jj + 2 == n)
                             mma_commit(bar(ctrl->q_empty));
                     }
-                    ++pcnt;
                 }
-                ++qcnt;
+                __syncwarp();
+                ++vcnt;
+                if (more)
+                    ++kcnt;
+                ++pcnt;
             }
-            // every MMA issued so far completes before TMEM and shared memory go
-            mma_commit(bar(ctrl->final_bar));
-            wait_drain(bar(ctrl->final_bar), 0, tmo);
+            ++qcnt;
         }
+        // every MMA issued so far completes before TMEM and shared memory go
+        if (leader)
+            mma_commit(bar(ctrl->final_bar));
+        __syncwarp();
+        wait_drain(bar(ctrl->final_bar), 0, tmo);
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax
         const int t = (warp - 4) >> 2;
