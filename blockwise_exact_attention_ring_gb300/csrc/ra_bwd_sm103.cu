@@ -325,48 +325,67 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dkdv_kernel(const __gri
         (void)ok;
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t sK = sb + C::KV_OFF_K, sV = sb + C::KV_OFF_V;
-            const int T = dkdv_count(j, tb, p);
-            auto sQ = [&](int n) { return sb + C::KV_OFF_Q + (n & 1) * C::TILE; };
-            auto sDO = [&](int n) { return sb + C::KV_OFF_DO + (n & 1) * C::TILE; };
-            bool ok = bwait(p.status, bar(ctrl->once_full), 0, abort, tmo, BS_KV_FULL);
-            if (ok && T > 0) {
-                if ((ok = bwait(p.status, bar(ctrl->st_full[0]), 0, abort, tmo, BS_ST_FULL))) {
-                    tc_fence_after();
-                    issue_rows_dot<D>(tmem, sK, sQ(0));        // S^T(0) = K Q^T
+        // The whole warp runs the loop on warp-uniform values, waits included;
+        // one lane, elected once, issues every MMA and commit (as in the
+        // forward kernel: the pipe idles while the issuing thread does
+        // anything else, and waits cost least in converged, uniform code).
+        const bool leader = elect_one();
+        const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
+        const uint32_t sK = sb + C::KV_OFF_K, sV = sb + C::KV_OFF_V;
+        const int T = dkdv_count(j, tb, p);
+        auto sQ = [&](int n) { return sb + C::KV_OFF_Q + (n & 1) * C::TILE; };
+        auto sDO = [&](int n) { return sb + C::KV_OFF_DO + (n & 1) * C::TILE; };
+        auto ww = [&](uint32_t bb, uint32_t parity, unsigned int site) {
+            return bwait_warp(p.status, bb, parity, abort, tmo, site);
+        };
+        bool ok = ww(bar(ctrl->once_full), 0, BS_KV_FULL);
+        if (ok && T > 0) {
+            if ((ok = ww(bar(ctrl->st_full[0]), 0, BS_ST_FULL))) {
+                tc_fence_after();
+                if (leader) {
+                    issue_rows_dot<D>(tm, sK, sQ(0));        // S^T(0) = K Q^T
                     mma_commit(bar(ctrl->s_full[0]));
-                    issue_rows_dot<D>(tmem + 128, sV, sDO(0));  // dP^T(0) = V dO^T
+                    issue_rows_dot<D>(tm + 128, sV, sDO(0));  // dP^T(0) = V dO^T
                     mma_commit(bar(ctrl->dp_full));
                 }
+                __syncwarp();
             }
-            for (int n = 0; ok && n < T; ++n) {
-                const bool next = n + 1 < T;
-                if (!(ok = bwait(p.status, bar(ctrl->p_full), n & 1, abort, tmo, BS_P_FULL)))
+        }
+        for (int n = 0; ok && n < T; ++n) {
+            const bool next = n + 1 < T;
+            if (!(ok = ww(bar(ctrl->p_full), n & 1, BS_P_FULL)))
+                break;
+            tc_fence_after();
+            if (leader)
+                issue_tmem_times_tile<D>(tm + 256, tm, sDO(n), n > 0);  // dV += P^T dO
+            __syncwarp();
+            if (next) {
+                if (!(ok = ww(bar(ctrl->st_full[(n + 1) & 1]), ((n + 1) >> 1) & 1, BS_ST_FULL)))
                     break;
                 tc_fence_after();
-                issue_tmem_times_tile<D>(tmem + 256, tmem, sDO(n), n > 0);  // dV += P^T dO
-                if (next) {
-                    if (!(ok = bwait(p.status, bar(ctrl->st_full[(n + 1) & 1]), ((n + 1) >> 1) & 1, abort, tmo,
-                                     BS_ST_FULL)))
-                        break;
-                    tc_fence_after();
-                    issue_rows_dot<D>(tmem, sK, sQ(n + 1));  // S^T(n+1): P^T(n) consumed in order
+                if (leader) {
+                    issue_rows_dot<D>(tm, sK, sQ(n + 1));  // S^T(n+1): P^T(n) consumed in order
                     mma_commit(bar(ctrl->s_full[0]));
                 }
-                if (!(ok = bwait(p.status, bar(ctrl->ds_full), n & 1, abort, tmo, BS_S_FULL)))
-                    break;
-                tc_fence_after();
-                issue_tmem_times_tile<D>(tmem + 256 + D, tmem + 128, sQ(n), n > 0);  // dK += dS^T Q
+                __syncwarp();
+            }
+            if (!(ok = ww(bar(ctrl->ds_full), n & 1, BS_S_FULL)))
+                break;
+            tc_fence_after();
+            if (leader) {
+                issue_tmem_times_tile<D>(tm + 256 + D, tm + 128, sQ(n), n > 0);  // dK += dS^T Q
                 mma_commit(bar(ctrl->st_empty[n & 1]));
                 if (next) {
-                    issue_rows_dot<D>(tmem + 128, sV, sDO(n + 1));  // dP^T(n+1): dS^T(n) consumed in order
+                    issue_rows_dot<D>(tm + 128, sV, sDO(n + 1));  // dP^T(n+1): dS^T(n) consumed in order
                     mma_commit(bar(ctrl->dp_full));
                 }
             }
-            mma_commit(bar(ctrl->final_bar));
-            bdrain(p.status, bar(ctrl->final_bar), 0, tmo);
+            __syncwarp();
         }
+        if (leader)
+            mma_commit(bar(ctrl->final_bar));
+        __syncwarp();
+        bdrain(p.status, bar(ctrl->final_bar), 0, tmo);
     } else {
         // ------------------------------------------------------------ elementwise
         // Two warps per TMEM lane quarter: half h takes query columns
@@ -576,59 +595,76 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dq_kernel(const __grid_
                 bdrain(p.status, bar(ctrl->st_full[m & 1]), (m >> 1) & 1, tmo);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t sQ = sb + C::Q_OFF_Q, sDO = sb + C::Q_OFF_DO;
-            const int T = dq_count(i, ta, p);
-            auto sK = [&](int n) { return sb + C::Q_OFF_K + (n % C::Q_KST) * C::TILE; };
-            auto sV = [&](int n) { return sb + C::Q_OFF_V + (n & 1) * C::TILE; };
-            auto wait_k = [&](int n) {
-                return bwait(p.status, bar(ctrl->kf[n % C::Q_KST]), (n / C::Q_KST) & 1, abort, tmo, BS_ST_FULL);
-            };
-            auto wait_v = [&](int n) {
-                return bwait(p.status, bar(ctrl->st_full[n & 1]), (n >> 1) & 1, abort, tmo, BS_ST_FULL);
-            };
-            bool ok = bwait(p.status, bar(ctrl->once_full), 0, abort, tmo, BS_Q_FULL);
-            // S(0), dP(0), S(1)
-            for (int n = 0; ok && n < 2 && n < T; ++n) {
-                if (!(ok = wait_k(n)))
+        // MMA issuer: the whole warp on uniform values, one elected lane issues
+        const bool leader = elect_one();
+        const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
+        const uint32_t sQ = sb + C::Q_OFF_Q, sDO = sb + C::Q_OFF_DO;
+        const int T = dq_count(i, ta, p);
+        auto sK = [&](int n) { return sb + C::Q_OFF_K + (n % C::Q_KST) * C::TILE; };
+        auto sV = [&](int n) { return sb + C::Q_OFF_V + (n & 1) * C::TILE; };
+        auto ww = [&](uint32_t bb, uint32_t parity, unsigned int site) {
+            return bwait_warp(p.status, bb, parity, abort, tmo, site);
+        };
+        auto wait_k = [&](int n) { return ww(bar(ctrl->kf[n % C::Q_KST]), (n / C::Q_KST) & 1, BS_ST_FULL); };
+        auto wait_v = [&](int n) { return ww(bar(ctrl->st_full[n & 1]), (n >> 1) & 1, BS_ST_FULL); };
+        bool ok = ww(bar(ctrl->once_full), 0, BS_Q_FULL);
+        // S(0), dP(0), S(1)
+        for (int n = 0; ok && n < 2 && n < T; ++n) {
+            if (!(ok = wait_k(n)))
+                break;
+            tc_fence_after();
+            if (leader) {
+                issue_rows_dot<D>(tm + (n ? 384u : 0u), sQ, sK(n));
+                mma_commit(bar(ctrl->s_full[n]));
+            }
+            __syncwarp();
+            if (n == 0) {
+                if (!(ok = wait_v(0)))
                     break;
                 tc_fence_after();
-                issue_rows_dot<D>(tmem + (n ? 384u : 0u), sQ, sK(n));
-                mma_commit(bar(ctrl->s_full[n]));
-                if (n == 0) {
-                    if (!(ok = wait_v(0)))
-                        break;
-                    tc_fence_after();
-                    issue_rows_dot<D>(tmem + 128, sDO, sV(0));
+                if (leader) {
+                    issue_rows_dot<D>(tm + 128, sDO, sV(0));
                     mma_commit(bar(ctrl->dp_full));
                     mma_commit(bar(ctrl->st_empty[0]));
                 }
+                __syncwarp();
             }
-            for (int n = 0; ok && n < T; ++n) {
-                if (!(ok = bwait(p.status, bar(ctrl->p_full), n & 1, abort, tmo, BS_P_FULL)))
+        }
+        for (int n = 0; ok && n < T; ++n) {
+            if (!(ok = ww(bar(ctrl->p_full), n & 1, BS_P_FULL)))
+                break;
+            tc_fence_after();
+            if (n + 1 < T) {
+                if (!(ok = wait_v(n + 1)))
                     break;
                 tc_fence_after();
-                if (n + 1 < T) {
-                    if (!(ok = wait_v(n + 1)))
-                        break;
-                    tc_fence_after();
-                    issue_rows_dot<D>(tmem + 128, sDO, sV(n + 1));  // dP(n+1): dP(n) was read
+                if (leader) {
+                    issue_rows_dot<D>(tm + 128, sDO, sV(n + 1));  // dP(n+1): dP(n) was read
                     mma_commit(bar(ctrl->dp_full));
                     mma_commit(bar(ctrl->st_empty[(n + 1) & 1]));
                 }
-                issue_tmem_times_tile<D>(tmem + 256, tmem + ((n & 1) ? 384u : 0u), sK(n), n > 0);  // dQ += dS K
+                __syncwarp();
+            }
+            if (leader) {
+                issue_tmem_times_tile<D>(tm + 256, tm + ((n & 1) ? 384u : 0u), sK(n), n > 0);  // dQ += dS K
                 mma_commit(bar(ctrl->ke[n % C::Q_KST]));
-                if (n + 2 < T) {
-                    if (!(ok = wait_k(n + 2)))
-                        break;
-                    tc_fence_after();
-                    issue_rows_dot<D>(tmem + ((n & 1) ? 384u : 0u), sQ, sK(n + 2));  // dS(n) consumed in order
+            }
+            __syncwarp();
+            if (n + 2 < T) {
+                if (!(ok = wait_k(n + 2)))
+                    break;
+                tc_fence_after();
+                if (leader) {
+                    issue_rows_dot<D>(tm + ((n & 1) ? 384u : 0u), sQ, sK(n + 2));  // dS(n) consumed in order
                     mma_commit(bar(ctrl->s_full[n & 1]));
                 }
+                __syncwarp();
             }
-            mma_commit(bar(ctrl->final_bar));
-            bdrain(p.status, bar(ctrl->final_bar), 0, tmo);
         }
+        if (leader)
+            mma_commit(bar(ctrl->final_bar));
+        __syncwarp();
+        bdrain(p.status, bar(ctrl->final_bar), 0, tmo);
     } else {
         // Two warps per TMEM lane quarter, half h on key columns [64h, 64h + 64);
         // packed dS goes to columns [32h, 32h + 32) of the S buffer, which for
