@@ -40,6 +40,7 @@
 #include <atomic>
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -383,47 +384,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
             }
             __syncwarp();
             ++kcnt;
-            for (int jj = 0; jj < n; ++jj) {
-                const int vs = vcnt % C::VSTAGES;
+            // One key tile per step.  Inside a unit's walk K runs one tile ahead
+            // of V (kcnt = vcnt + 1), so with two stages each the K stage is
+            // the other one: the step is specialised on V's stage and every
+            // shared-memory address below is the base plus a constant.
+            static_assert(C::KSTAGES == 2 && C::VSTAGES == 2, "stage parity specialisation");
+            auto step = [&](auto vs_c, int jj) -> bool {
+                constexpr int VS = decltype(vs_c)::value, KS = 1 - VS;
                 const bool more = jj + 1 < n;
-                if (!(ok = kv_wwait(bar(ctrl->v_full[vs]), (vcnt / C::VSTAGES) & 1, SITE_V_FULL)))
-                    break;
-                if (jj == 0 && qcnt > 0 && !(ok = wwait(bar(ctrl->o_free[0]), (qcnt - 1) & 1, SITE_O_FREE)))
-                    break;
-                if (!(ok = wwait(bar(ctrl->p_full[0]), pcnt & 1, SITE_P_FULL)))
-                    break;
+                if (!kv_wwait(bar(ctrl->v_full[VS]), (vcnt >> 1) & 1, SITE_V_FULL))
+                    return false;
+                if (jj == 0 && qcnt > 0 && !wwait(bar(ctrl->o_free[0]), (qcnt - 1) & 1, SITE_O_FREE))
+                    return false;
+                if (!wwait(bar(ctrl->p_full[0]), pcnt & 1, SITE_P_FULL))
+                    return false;
                 tc_fence_after();
                 if (leader) {
-                    issue_pv(0, vs, jj > 0);
+                    issue_pv(0, VS, jj > 0);
                     if (!more)
                         mma_commit(bar(ctrl->o_done[0]));  // O of tile 0 complete for the unit
                 }
                 __syncwarp();
                 if (more) {
-                    ks = kcnt % C::KSTAGES;
-                    if (!(ok = kv_wwait(bar(ctrl->k_full[ks]), (kcnt / C::KSTAGES) & 1, SITE_K_FULL)))
-                        break;
+                    if (!kv_wwait(bar(ctrl->k_full[KS]), (kcnt >> 1) & 1, SITE_K_FULL))
+                        return false;
                     tc_fence_after();
                     if (leader) {
-                        issue_s(0, ks);
+                        issue_s(0, KS);
                         mma_commit(bar(ctrl->s_full[0]));
                     }
                     __syncwarp();
                 }
-                if (jj == 0 && qcnt > 0 && !(ok = wwait(bar(ctrl->o_free[1]), (qcnt - 1) & 1, SITE_O_FREE)))
-                    break;
-                if (!(ok = wwait(bar(ctrl->p_full[1]), pcnt & 1, SITE_P_FULL)))
-                    break;
+                if (jj == 0 && qcnt > 0 && !wwait(bar(ctrl->o_free[1]), (qcnt - 1) & 1, SITE_O_FREE))
+                    return false;
+                if (!wwait(bar(ctrl->p_full[1]), pcnt & 1, SITE_P_FULL))
+                    return false;
                 tc_fence_after();
                 if (leader) {
-                    issue_pv(1, vs, jj > 0);
+                    issue_pv(1, VS, jj > 0);
                     if (!more)
                         mma_commit(bar(ctrl->o_done[1]));  // O of tile 1 complete for the unit
-                    kv_release(bar(ctrl->v_empty[vs]));
+                    kv_release(bar(ctrl->v_empty[VS]));
                     if (more) {
-                        issue_s(1, ks);
+                        issue_s(1, KS);
                         mma_commit(bar(ctrl->s_full[1]));
-                        kv_release(bar(ctrl->k_empty[ks]));
+                        kv_release(bar(ctrl->k_empty[KS]));
                         if (jj + 2 == n)
                             mma_commit(bar(ctrl->q_empty));
                     }
@@ -433,7 +438,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
                 if (more)
                     ++kcnt;
                 ++pcnt;
-            }
+                return true;
+            };
+            for (int jj = 0; ok && jj < n; ++jj)
+                ok = (vcnt & 1) ? step(std::integral_constant<int, 1>{}, jj) : step(std::integral_constant<int, 0>{}, jj);
             ++qcnt;
         }
         // every MMA issued so far completes before TMEM and shared memory go
