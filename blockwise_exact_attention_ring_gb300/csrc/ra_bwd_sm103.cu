@@ -94,7 +94,6 @@ struct BwdCtrl {
     uint64_t dp_full;              // dP
     uint64_t p_full;               // dK/dV: P^T written; dQ: dS written (256 arrivals)
     uint64_t ds_full;              // dK/dV: dS^T written (256 arrivals)
-    uint64_t pair[4];              // the two warps of a TMEM lane quarter (64 arrivals)
     uint64_t final_bar;
     uint32_t tmem_base;
     int abort;
@@ -167,6 +166,15 @@ __device__ __forceinline__ void issue_rows_dot(uint32_t d_tmem, uint32_t a, uint
 }
 
 // D (+)= A[tmem, 128 x 128 bf16] B, B a [128 rows = K][D] tile read MN-major.
+// A is packed by the two halves of the elementwise warps: K columns
+// [64h, 64h + 64) of A (32 TMEM columns of bf16 pairs) sit at TMEM columns
+// [64h + 32, 64h + 64) of the 128-column region at a_tmem, the upper half of
+// the columns that half h itself loaded its inputs from.
+__device__ __forceinline__ uint32_t packed_col(int kk)
+{
+    return (uint32_t)((kk >> 2) * 64 + 32 + (kk & 3) * 8);
+}
+
 template <int D>
 __device__ __forceinline__ void issue_tmem_times_tile(uint32_t d_tmem, uint32_t a_tmem, uint32_t b,
                                                       bool accumulate)
@@ -174,7 +182,7 @@ __device__ __forceinline__ void issue_tmem_times_tile(uint32_t d_tmem, uint32_t 
     constexpr uint32_t ID = idesc_bf16_f32(128, D, 1);
 #pragma unroll
     for (int kk = 0; kk < RA_TILE / 16; ++kk)
-        mma_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128(b + kk * 2048, BwdCfg<D>::SLAB, 1024), ID,
+        mma_ts(d_tmem, a_tmem + packed_col(kk), smem_desc_sw128(b + kk * 2048, BwdCfg<D>::SLAB, 1024), ID,
                (accumulate || kk > 0) ? 1u : 0u);
 }
 
@@ -214,8 +222,6 @@ __device__ __forceinline__ void bwd_init_barriers(BwdCtrl *ctrl)
     mbar_init(smem_u32(&ctrl->dp_full), 1);
     mbar_init(smem_u32(&ctrl->p_full), BWD_EW);
     mbar_init(smem_u32(&ctrl->ds_full), BWD_EW);
-    for (int q = 0; q < 4; ++q)
-        mbar_init(smem_u32(&ctrl->pair[q]), 64);
     mbar_init(smem_u32(&ctrl->final_bar), 1);
     ctrl->abort = 0;
     fence_mbar_init();
@@ -389,9 +395,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dkdv_kernel(const __gri
     } else {
         // ------------------------------------------------------------ elementwise
         // Two warps per TMEM lane quarter: half h takes query columns
-        // [64h, 64h + 64).  Its packed P^T / dS^T land in columns [32h, 32h + 32)
-        // of the S^T / dP^T region, which for h = 1 hold half 0's inputs: the
-        // halves meet at pair[quarter] after loading and before storing.
+        // [64h, 64h + 64).  Its packed P^T / dS^T land in columns
+        // [64h + 32, 64h + 64) of the S^T / dP^T region, inside the columns it
+        // loaded itself, so the halves never wait for each other.
         const int qw = warp & 3;
         const int h = (warp - 2) >> 2;
         const int r = qw * 32 + lane;                 // key row of the tile
@@ -400,17 +406,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dkdv_kernel(const __gri
         const int bl = tb * RA_TILE + r;              // key local index in block j
         const bool key_ok = bl < p.L;
         const float sl2 = p.scale_log2;
-        const uint32_t pair = bar(ctrl->pair[qw]);
-        uint32_t n = 0, npair = 0;
+        uint32_t n = 0;
         bool ok = true;
-        auto meet = [&]() -> bool {
-            tc_fence_before();
-            mbar_arrive(pair);
-            const bool met = bwait_warp(p.status, pair, npair & 1, abort, tmo, BS_S_FULL);
-            ++npair;
-            tc_fence_after();
-            return met;
-        };
         RaQWalk w;
         w.start(j, tb, p.N, p.layout, p.causal, p.ntiles, grp);
         for (; w.valid(); w.advance(), ++n) {
@@ -428,8 +425,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dkdv_kernel(const __gri
             uint32_t xs[64], pp[32];
             tmem_ld64(tS + 64 * h, xs);
             tmem_wait_ld();
-            if (!(ok = meet()))
-                break;
             // P^T = 2^(S^T c log2e - lse log2e), masked where some query of the
             // warp's half-tile does not see the warp's keys
             const float2 sl2x2 = make_float2(sl2, sl2);
@@ -452,7 +447,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dkdv_kernel(const __gri
                     pp[e >> 1] = pack_bf16x2(p0, p1);
                 }
             }
-            tmem_st32(tS + 32 * h, pp);
+            tmem_st32(tS + 64 * h + 32, pp);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(ctrl->p_full));
@@ -463,8 +458,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dkdv_kernel(const __gri
             uint32_t xd[64], pd[32];
             tmem_ld64(tP + 64 * h, xd);
             tmem_wait_ld();
-            if (!(ok = meet()))
-                break;
             const float2 *dl2 = reinterpret_cast<const float2 *>(dl);
             const float2 zero2 = make_float2(0.f, 0.f);
 #pragma unroll
@@ -476,7 +469,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dkdv_kernel(const __gri
                 const float2 ds = ffma2(make_float2(bf16_lo(pk), bf16_hi(pk)), t, zero2);
                 pd[e >> 1] = pack_bf16x2(ds.x, ds.y);
             }
-            tmem_st32(tP + 32 * h, pd);
+            tmem_st32(tP + 64 * h + 32, pd);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(ctrl->ds_full));
@@ -667,8 +660,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dq_kernel(const __grid_
         bdrain(p.status, bar(ctrl->final_bar), 0, tmo);
     } else {
         // Two warps per TMEM lane quarter, half h on key columns [64h, 64h + 64);
-        // packed dS goes to columns [32h, 32h + 32) of the S buffer, which for
-        // h = 1 still hold half 0's scores until the halves meet at pair[quarter].
+        // packed dS goes to columns [64h + 32, 64h + 64) of the S buffer, inside
+        // the columns half h loaded its scores from: the halves never wait for
+        // each other.
         const int qw = warp & 3;
         const int h = (warp - 2) >> 2;
         const int r = qw * 32 + lane;
@@ -680,7 +674,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dq_kernel(const __grid_
         const float nl = row_ok ? -p.lse[grow] * LOG2E : 0.f;
         const float dl = row_ok ? p.delta[grow] : 0.f;
         const float sl2 = p.scale_log2;
-        const uint32_t pair = bar(ctrl->pair[qw]);
         uint32_t n = 0;
         bool ok = true;
         RaKWalk w;
@@ -696,11 +689,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dq_kernel(const __grid_
             uint32_t xs[64];
             tmem_ld64(tS + 64 * h, xs);
             tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(pair);
-            if (!(ok = bwait_warp(p.status, pair, n & 1, abort, tmo, BS_S_FULL)))
-                break;
-            tc_fence_after();
             uint32_t pd[32];
             const float2 sl2x2 = make_float2(sl2, sl2), nl2 = make_float2(nl, nl), ndl2 = make_float2(-dl, -dl);
             const float2 zero2 = make_float2(0.f, 0.f);
@@ -724,7 +712,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dq_kernel(const __grid_
                     pd[x >> 1] = pack_bf16x2(ds.x, ds.y);
                 }
             }
-            tmem_st32(tS + 32 * h, pd);
+            tmem_st32(tS + 64 * h + 32, pd);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(ctrl->p_full));
