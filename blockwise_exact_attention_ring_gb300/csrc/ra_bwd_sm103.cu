@@ -295,6 +295,16 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dkdv_kernel(const __gri
             const int st = n & 1;
             const int bh = b * p.H + g * grp + w.hh;
             const long long row0 = (long long)bh * p.S + (long long)w.i * p.L + w.ta * RA_TILE;
+            // the tile's -lse log2e and delta rows: loaded before the stage
+            // wait, so that their latency overlaps it
+            float nlv[4], dlv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = lane + 32 * e;
+                const bool valid = w.ta * RA_TILE + r < p.L;
+                nlv[e] = valid ? -p.lse[row0 + r] * LOG2E : 0.f;
+                dlv[e] = valid ? p.delta[row0 + r] : 0.f;
+            }
             if (n >= 2) {
                 if (lane == 0) {
                     // the stage frees only after dK(n - 2): have the tiles in L2 by then
@@ -305,21 +315,23 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dkdv_kernel(const __gri
                                       BS_ST_EMPTY)))
                     break;
             }
+            // the copies go out first; the stage's one arrival follows the row
+            // stores, so the phase completes with both the bytes and the rows
+            const uint32_t full = bar(ctrl->st_full[st]);
+            if (lane == 0) {
+                mbar_expect_tx(full, 2 * C::TILE);
+                bload_tile<D>(sb + C::KV_OFF_Q + st * C::TILE, &p.tm_q, (int)row0, full, pol_q);
+                bload_tile<D>(sb + C::KV_OFF_DO + st * C::TILE, &p.tm_do, (int)row0, full, pol_q);
+            }
             float *nl = rows + st * 256, *dl = nl + 128;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int r = lane + 32 * e;
-                const bool valid = w.ta * RA_TILE + r < p.L;
-                nl[r] = valid ? -p.lse[row0 + r] * LOG2E : 0.f;
-                dl[r] = valid ? p.delta[row0 + r] : 0.f;
+                nl[lane + 32 * e] = nlv[e];
+                dl[lane + 32 * e] = dlv[e];
             }
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive_expect_tx(bar(ctrl->st_full[st]), 2 * C::TILE);
-                bload_tile<D>(sb + C::KV_OFF_Q + st * C::TILE, &p.tm_q, (int)row0, bar(ctrl->st_full[st]), pol_q);
-                bload_tile<D>(sb + C::KV_OFF_DO + st * C::TILE, &p.tm_do, (int)row0, bar(ctrl->st_full[st]),
-                              pol_q);
-            }
+            if (lane == 0)
+                mbar_arrive(full);
             __syncwarp();
         }
         if (lane == 0) {

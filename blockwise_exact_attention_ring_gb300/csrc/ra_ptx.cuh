@@ -59,6 +59,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  ::"r"(bar), "r"(bytes) : "memory");
 }
 
+// Raises the transaction count of the current phase without arriving: the
+// phase then also waits for an arrival made later (for instance after data
+// that travels with the phase has been stored).
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
