@@ -249,73 +249,85 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            const uint64_t pol_q = l2_policy_evict_first();
-            const uint64_t pol_kv = l2_policy_evict_last();
-            uint32_t kcnt = 0, vcnt = 0, qcnt = 0;
-            bool ok = true;
-            for (int r = 0; ok; ++r) {
-                const int wi = unit_of(r);
-                if (wi >= p.n_items)
-                    break;
-                int k = 0, t0 = 0, cnt = 0;
-                const RaUnit U = SPLIT ? item_decode(p, wi, k, t0, cnt) : ra_unit_decode(p.sp, wi);
-                if (SPLIT && cnt == 0)
-                    continue;  // an empty piece: nothing to load
-                if (qcnt > 0 && !(ok = wait1(bar(ctrl->q_empty), (qcnt - 1) & 1, abort, tmo,
-                                                 SITE_Q_EMPTY)))
-                    break;
+        // The whole warp runs the loop on warp-uniform values, its waits
+        // included (a wait costs less in converged code, and each one sits on
+        // the path from a freed stage to its next copy); one lane, elected
+        // once, arms the barriers and issues the copies.
+        const bool leader = elect_one();
+        const uint64_t pol_q = l2_policy_evict_first();
+        const uint64_t pol_kv = l2_policy_evict_last();
+        auto pwait = [&](uint32_t b, uint32_t parity, unsigned int site) -> bool {
+            return __all_sync(0xffffffffu, kv_wait(b, parity, site)) != 0;
+        };
+        uint32_t kcnt = 0, vcnt = 0, qcnt = 0;
+        bool ok = true;
+        for (int r = 0; ok; ++r) {
+            const int wi = unit_of(r);
+            if (wi >= p.n_items)
+                break;
+            int k = 0, t0 = 0, cnt = 0;
+            const RaUnit U = SPLIT ? item_decode(p, wi, k, t0, cnt) : ra_unit_decode(p.sp, wi);
+            if (SPLIT && cnt == 0)
+                continue;  // an empty piece: nothing to load
+            if (qcnt > 0 && !(ok = wait_warp(bar(ctrl->q_empty), (qcnt - 1) & 1, abort, tmo, SITE_Q_EMPTY)))
+                break;
+            if (leader) {
                 mbar_arrive_expect_tx(bar(ctrl->q_full), 2 * C::TILE);
                 const int qrow0 = U.bh0 * p.S + U.rank * p.L + U.ta0 * RA_TILE;
                 const int qrow1 = U.bh1 * p.S + U.rank * p.L + U.ta1 * RA_TILE;
                 load_tile<D>(sQ, &p.tm_q, qrow0, bar(ctrl->q_full), pol_q);
                 load_tile<D>(sQ + C::TILE, &p.tm_q, qrow1, bar(ctrl->q_full), pol_q);
-                ++qcnt;
-                const int b = U.bh0 / p.H;
-                const int kvbh = b * p.Hkv + (U.bh0 - b * p.H) / group;
-                KvWalk w;
-                w.start(U.rank, max(U.ta0, U.ta1), p);
-                if (SPLIT)
-                    w.skip(t0);
-                for (int c = 0; SPLIT ? c < cnt : w.valid(); ++c, w.advance()) {
-                    const int row = kvbh * p.S + w.j * p.L + w.tb * RA_TILE;
-                    const int ks = kcnt % C::KSTAGES;
-                    if (!(ok = kv_wait(bar(ctrl->k_empty[ks]), ((kcnt / C::KSTAGES) & 1) ^ 1,
-                                       SITE_K_EMPTY)))
-                        break;
+            }
+            __syncwarp();
+            ++qcnt;
+            const int b = U.bh0 / p.H;
+            const int kvbh = b * p.Hkv + (U.bh0 - b * p.H) / group;
+            KvWalk w;
+            w.start(U.rank, max(U.ta0, U.ta1), p);
+            if (SPLIT)
+                w.skip(t0);
+            for (int c = 0; SPLIT ? c < cnt : w.valid(); ++c, w.advance()) {
+                const int row = kvbh * p.S + w.j * p.L + w.tb * RA_TILE;
+                const int ks = kcnt % C::KSTAGES;
+                if (!(ok = pwait(bar(ctrl->k_empty[ks]), ((kcnt / C::KSTAGES) & 1) ^ 1, SITE_K_EMPTY)))
+                    break;
+                if (leader) {
                     mbar_arrive_expect_tx(bar(ctrl->k_full[ks]), C::TILE);
                     if (CL == 1)
                         load_tile<D>(sK + ks * C::TILE, &p.tm_k, row, bar(ctrl->k_full[ks]), pol_kv);
                     else if (crank == 0)
                         load_tile_both<D>(sK + ks * C::TILE, &p.tm_k, row, bar(ctrl->k_full[ks]), pol_kv);
-                    ++kcnt;
-                    const int vs = vcnt % C::VSTAGES;
-                    if (!(ok = kv_wait(bar(ctrl->v_empty[vs]), ((vcnt / C::VSTAGES) & 1) ^ 1,
-                                       SITE_V_EMPTY)))
-                        break;
+                }
+                __syncwarp();
+                ++kcnt;
+                const int vs = vcnt % C::VSTAGES;
+                if (!(ok = pwait(bar(ctrl->v_empty[vs]), ((vcnt / C::VSTAGES) & 1) ^ 1, SITE_V_EMPTY)))
+                    break;
+                if (leader) {
                     mbar_arrive_expect_tx(bar(ctrl->v_full[vs]), C::TILE);
                     if (CL == 1)
                         load_tile<D>(sV + vs * C::TILE, &p.tm_v, row, bar(ctrl->v_full[vs]), pol_kv);
                     else if (crank == 1)
                         load_tile_both<D>(sV + vs * C::TILE, &p.tm_v, row, bar(ctrl->v_full[vs]), pol_kv);
-                    ++vcnt;
                 }
+                __syncwarp();
+                ++vcnt;
             }
-            if (!ok) {
-                // let every issued copy land before shared memory is released
-                for (int s = 0; s < C::KSTAGES; ++s) {
-                    const uint32_t n = kcnt > (uint32_t)s ? (kcnt - s + C::KSTAGES - 1) / C::KSTAGES : 0;
-                    if (n)
-                        wait_drain(bar(ctrl->k_full[s]), (n - 1) & 1, tmo);
-                }
-                for (int s = 0; s < C::VSTAGES; ++s) {
-                    const uint32_t n = vcnt > (uint32_t)s ? (vcnt - s + C::VSTAGES - 1) / C::VSTAGES : 0;
-                    if (n)
-                        wait_drain(bar(ctrl->v_full[s]), (n - 1) & 1, tmo);
-                }
-                if (qcnt)
-                    wait_drain(bar(ctrl->q_full), (qcnt - 1) & 1, tmo);
+        }
+        if (!ok) {
+            // let every issued copy land before shared memory is released
+            for (int s = 0; s < C::KSTAGES; ++s) {
+                const uint32_t n = kcnt > (uint32_t)s ? (kcnt - s + C::KSTAGES - 1) / C::KSTAGES : 0;
+                if (n)
+                    wait_drain(bar(ctrl->k_full[s]), (n - 1) & 1, tmo);
             }
+            for (int s = 0; s < C::VSTAGES; ++s) {
+                const uint32_t n = vcnt > (uint32_t)s ? (vcnt - s + C::VSTAGES - 1) / C::VSTAGES : 0;
+                if (n)
+                    wait_drain(bar(ctrl->v_full[s]), (n - 1) & 1, tmo);
+            }
+            if (qcnt)
+                wait_drain(bar(ctrl->q_full), (qcnt - 1) & 1, tmo);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer

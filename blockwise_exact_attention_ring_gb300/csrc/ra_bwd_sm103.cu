@@ -114,12 +114,6 @@ struct BwdParams {
 
 // Waits record a timeout in the library's status word (`st`, passed in by
 // the launch).
-__device__ __forceinline__ bool bwait(unsigned int *st, uint32_t bar, uint32_t parity, volatile int *abort,
-                                      uint64_t tmo, unsigned int site)
-{
-    return mbar_wait(bar, parity, abort, tmo, st, site);
-}
-
 __device__ __forceinline__ bool bwait_warp(unsigned int *st, uint32_t bar, uint32_t parity, volatile int *abort,
                                            uint64_t tmo, unsigned int site)
 {
@@ -557,48 +551,61 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dq_kernel(const __grid_
     const uint64_t tmo = p.timeout_ns;
 
     if (warp == 0) {
-        if (lane == 0) {
-            const uint64_t pol_q = l2_policy_evict_first();
-            const uint64_t pol_kv = l2_policy_evict_last();
+        // producer: the whole warp on uniform values (its waits sit on the path
+        // from a freed stage to the next copy), one elected lane issues
+        const bool leader = elect_one();
+        const uint64_t pol_q = l2_policy_evict_first();
+        const uint64_t pol_kv = l2_policy_evict_last();
+        if (leader) {
             mbar_arrive_expect_tx(bar(ctrl->once_full), 2 * C::TILE);
             bload_tile<D>(sb + C::Q_OFF_Q, &p.tm_q, qrow, bar(ctrl->once_full), pol_q);
             bload_tile<D>(sb + C::Q_OFF_DO, &p.tm_do, qrow, bar(ctrl->once_full), pol_q);
-            uint32_t n = 0;
-            bool ok = true;
-            RaKWalk w;
-            w.start(i, ta, p.N, p.layout, p.causal, p.ntiles);
-            uint32_t nk = 0, nv = 0;  // K and V loads issued
-            for (; w.valid(); w.advance(), ++n) {
-                const int ks = n % C::Q_KST, vs = n & 1;
-                const int row = kvbh * p.S + w.j * p.L + w.tb * RA_TILE;
-                if (n >= (uint32_t)C::Q_KST) {
-                    // K's stage frees after dQ(n - 3): have the tile in L2 by then
+        }
+        __syncwarp();
+        uint32_t n = 0;
+        bool ok = true;
+        RaKWalk w;
+        w.start(i, ta, p.N, p.layout, p.causal, p.ntiles);
+        uint32_t nk = 0, nv = 0;  // K and V loads issued
+        for (; w.valid(); w.advance(), ++n) {
+            const int ks = n % C::Q_KST, vs = n & 1;
+            const int row = kvbh * p.S + w.j * p.L + w.tb * RA_TILE;
+            if (n >= (uint32_t)C::Q_KST) {
+                // K's stage frees after dQ(n - 3): have the tile in L2 by then
+                if (leader)
                     bprefetch_tile<D>(&p.tm_k, row);
-                    if (!(ok = bwait(p.status, bar(ctrl->ke[ks]), (n / C::Q_KST - 1) & 1, abort, tmo,
-                                     BS_KV_EMPTY)))
-                        break;
-                }
+                if (!(ok = bwait_warp(p.status, bar(ctrl->ke[ks]), (n / C::Q_KST - 1) & 1, abort, tmo,
+                                      BS_KV_EMPTY)))
+                    break;
+            }
+            if (leader) {
                 mbar_arrive_expect_tx(bar(ctrl->kf[ks]), C::TILE);
                 bload_tile<D>(sb + C::Q_OFF_K + ks * C::TILE, &p.tm_k, row, bar(ctrl->kf[ks]), pol_kv);
-                ++nk;
-                if (n >= 2) {
-                    // V's stage frees once dP(n - 2) has read it
+            }
+            __syncwarp();
+            ++nk;
+            if (n >= 2) {
+                // V's stage frees once dP(n - 2) has read it
+                if (leader)
                     bprefetch_tile<D>(&p.tm_v, row);
-                    if (!(ok = bwait(p.status, bar(ctrl->st_empty[vs]), ((n >> 1) - 1) & 1, abort, tmo,
-                                     BS_KV_EMPTY)))
-                        break;
-                }
+                if (!(ok = bwait_warp(p.status, bar(ctrl->st_empty[vs]), ((n >> 1) - 1) & 1, abort, tmo,
+                                      BS_KV_EMPTY)))
+                    break;
+            }
+            if (leader) {
                 mbar_arrive_expect_tx(bar(ctrl->st_full[vs]), C::TILE);
                 bload_tile<D>(sb + C::Q_OFF_V + vs * C::TILE, &p.tm_v, row, bar(ctrl->st_full[vs]), pol_kv);
-                ++nv;
             }
-            // every issued copy lands before shared memory is released
-            bdrain(p.status, bar(ctrl->once_full), 0, tmo);
-            for (uint32_t m = nk > (uint32_t)C::Q_KST ? nk - C::Q_KST : 0; m < nk; ++m)
-                bdrain(p.status, bar(ctrl->kf[m % C::Q_KST]), (m / C::Q_KST) & 1, tmo);
-            for (uint32_t m = nv > 2 ? nv - 2 : 0; m < nv; ++m)
-                bdrain(p.status, bar(ctrl->st_full[m & 1]), (m >> 1) & 1, tmo);
+            __syncwarp();
+            ++nv;
         }
+        // every issued copy lands before shared memory is released
+        bdrain(p.status, bar(ctrl->once_full), 0, tmo);
+        for (uint32_t m = nk > (uint32_t)C::Q_KST ? nk - C::Q_KST : 0; m < nk; ++m)
+            bdrain(p.status, bar(ctrl->kf[m % C::Q_KST]), (m / C::Q_KST) & 1, tmo);
+        for (uint32_t m = nv > 2 ? nv - 2 : 0; m < nv; ++m)
+            bdrain(p.status, bar(ctrl->st_full[m & 1]), (m >> 1) & 1, tmo);
+        (void)ok;
     } else if (warp == 1) {
         // MMA issuer: the whole warp on uniform values, one elected lane issues
         const bool leader = elect_one();
