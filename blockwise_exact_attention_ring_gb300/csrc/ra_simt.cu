@@ -572,53 +572,82 @@ void launch_finalize(const float *run, const float *run_lse, void *out, float *l
 // key and is not read.  The same running-softmax merge as ra_merge_kernel,
 // over nsplit partials at once.
 template <typename OUT>
+__device__ __forceinline__ void combine_row_vector(const float *__restrict__ part, const float *__restrict__ part_lse,
+                                                   int nsplit, long long part_stride, OUT *__restrict__ out,
+                                                   float *__restrict__ lse, long long row, int c4, long long drow,
+                                                   int d)
+{
+    float m = -INFINITY;
+    for (int k = 0; k < nsplit; ++k)
+        m = fmaxf(m, __ldg(part_lse + k * part_stride + row));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float sum = 0.f;
+    if (m != -INFINITY) {
+        for (int k = 0; k < nsplit; ++k) {
+            const float lk = __ldg(part_lse + k * part_stride + row);
+            if (lk == -INFINITY)
+                continue;
+            const float wk = expf(lk - m);
+            const float4 x = __ldg(reinterpret_cast<const float4 *>(part + (k * part_stride + row) * d) + c4);
+            acc.x += wk * x.x;
+            acc.y += wk * x.y;
+            acc.z += wk * x.z;
+            acc.w += wk * x.w;
+            sum += wk;
+        }
+        const float inv = 1.f / sum;
+        acc.x *= inv, acc.y *= inv, acc.z *= inv, acc.w *= inv;
+    }
+    if constexpr (sizeof(OUT) == 4) {
+        reinterpret_cast<float4 *>(out + drow * d)[c4] = acc;
+    } else {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 w;
+        w.x = *reinterpret_cast<uint32_t *>(&lo);
+        w.y = *reinterpret_cast<uint32_t *>(&hi);
+        reinterpret_cast<uint2 *>(out + drow * d)[c4] = w;
+    }
+    if (c4 == 0)
+        lse[drow] = m == -INFINITY ? -INFINITY : m + logf(sum);
+}
+
+// One thread per 16-byte vector of an output row.  NARROW: every vector
+// index is below 2^31, and the row, head and position come from 32-bit
+// division by invariant integers; otherwise 64-bit arithmetic.
+template <typename OUT, bool NARROW>
 __global__ void ra_combine_kernel(const float *__restrict__ part, const float *__restrict__ part_lse, int nsplit,
                                   long long part_stride, OUT *__restrict__ out, float *__restrict__ lse,
-                                  long long rows_total, int S, int L, int N, int striped, int d)
+                                  long long rows_total, int S, int L, int N, int striped, int d, FastDiv fv,
+                                  FastDiv fS, FastDiv fL)
 {
     const int vpr = d / 4;  // 16-byte vectors per row
-    const long long n = rows_total * vpr;
-    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
-         idx += (long long)gridDim.x * blockDim.x) {
-        const long long row = idx / vpr;
-        const int c4 = (int)(idx - row * vpr);
-        float m = -INFINITY;
-        for (int k = 0; k < nsplit; ++k)
-            m = fmaxf(m, part_lse[k * part_stride + row]);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        float sum = 0.f;
-        if (m != -INFINITY) {
-            for (int k = 0; k < nsplit; ++k) {
-                const float lk = part_lse[k * part_stride + row];
-                if (lk == -INFINITY)
-                    continue;
-                const float wk = expf(lk - m);
-                const float4 x = reinterpret_cast<const float4 *>(part + (k * part_stride + row) * d)[c4];
-                acc.x += wk * x.x;
-                acc.y += wk * x.y;
-                acc.z += wk * x.z;
-                acc.w += wk * x.w;
-                sum += wk;
+    if (NARROW) {
+        const uint32_t n = (uint32_t)(rows_total * vpr);
+        for (uint32_t idx = blockIdx.x * blockDim.x + threadIdx.x; idx < n; idx += gridDim.x * blockDim.x) {
+            const uint32_t row = fdiv(idx, fv);
+            const int c4 = (int)(idx - row * (uint32_t)vpr);
+            const uint32_t bh = fdiv(row, fS);
+            const uint32_t p = row - bh * (uint32_t)S;
+            uint32_t t = p;
+            if (striped) {
+                const uint32_t r = fdiv(p, fL);
+                t = (p - r * (uint32_t)L) * (uint32_t)N + r;
             }
-            const float inv = 1.f / sum;
-            acc.x *= inv, acc.y *= inv, acc.z *= inv, acc.w *= inv;
+            combine_row_vector<OUT>(part, part_lse, nsplit, part_stride, out, lse, row, c4,
+                                    (long long)bh * S + t, d);
         }
-        const long long bh = row / S;
-        const int p = (int)(row - bh * S);
-        const int t = striped ? (p % L) * N + p / L : p;
-        const long long drow = bh * S + t;
-        if constexpr (sizeof(OUT) == 4) {
-            reinterpret_cast<float4 *>(out + drow * d)[c4] = acc;
-        } else {
-            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-            __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-            uint2 w;
-            w.x = *reinterpret_cast<uint32_t *>(&lo);
-            w.y = *reinterpret_cast<uint32_t *>(&hi);
-            reinterpret_cast<uint2 *>(out + drow * d)[c4] = w;
+    } else {
+        const long long n = rows_total * vpr;
+        for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
+             idx += (long long)gridDim.x * blockDim.x) {
+            const long long row = idx / vpr;
+            const int c4 = (int)(idx - row * vpr);
+            const long long bh = row / S;
+            const int p = (int)(row - bh * S);
+            const int t = striped ? (p % L) * N + p / L : p;
+            combine_row_vector<OUT>(part, part_lse, nsplit, part_stride, out, lse, row, c4, bh * S + t, d);
         }
-        if (c4 == 0)
-            lse[drow] = m == -INFINITY ? -INFINITY : m + logf(sum);
     }
 }
 
@@ -634,12 +663,25 @@ void launch_combine(const float *part, const float *part_lse, int nsplit, long l
     if (blocks < 1)
         blocks = 1;
     const int L = S / N;
-    if (out_bf16)
-        ra_combine_kernel<__nv_bfloat16><<<(int)blocks, threads, 0, st>>>(
-            part, part_lse, nsplit, part_stride, (__nv_bfloat16 *)out, lse, rows_total, S, L, N, striped, d);
-    else
-        ra_combine_kernel<float><<<(int)blocks, threads, 0, st>>>(
-            part, part_lse, nsplit, part_stride, (float *)out, lse, rows_total, S, L, N, striped, d);
+    const bool narrow = rows_total * (d / 4) < (1ll << 31);
+    const FastDiv fv = make_fastdiv((uint32_t)(d / 4)), fS = make_fastdiv((uint32_t)S), fL = make_fastdiv((uint32_t)L);
+    if (out_bf16) {
+        auto *o = (__nv_bfloat16 *)out;
+        if (narrow)
+            ra_combine_kernel<__nv_bfloat16, true><<<(int)blocks, threads, 0, st>>>(
+                part, part_lse, nsplit, part_stride, o, lse, rows_total, S, L, N, striped, d, fv, fS, fL);
+        else
+            ra_combine_kernel<__nv_bfloat16, false><<<(int)blocks, threads, 0, st>>>(
+                part, part_lse, nsplit, part_stride, o, lse, rows_total, S, L, N, striped, d, fv, fS, fL);
+    } else {
+        auto *o = (float *)out;
+        if (narrow)
+            ra_combine_kernel<float, true><<<(int)blocks, threads, 0, st>>>(
+                part, part_lse, nsplit, part_stride, o, lse, rows_total, S, L, N, striped, d, fv, fS, fL);
+        else
+            ra_combine_kernel<float, false><<<(int)blocks, threads, 0, st>>>(
+                part, part_lse, nsplit, part_stride, o, lse, rows_total, S, L, N, striped, d, fv, fS, fL);
+    }
 }
 
 }  // namespace ra
