@@ -239,12 +239,40 @@ ra_status attention_pass(const Problem &p, const void *q, const void *k, const v
     a.nsplit = nsplit;
     a.split_out_bytes = (long long)p.q_elems() * 4;
     a.split_lse_stride = (long long)p.rows();
-    if (ra_unit_count(ra_unit_space_ranks(ra_unit_space(p.B, p.H, p.Hkv, p.S, p.N, p.layout, p.causal,
-                                                        s_begin, s_end),
-                                          rank_lo, rank_hi)) > 0)
-        count_launch();
+    const RaUnitSpace sp = ra_unit_space_ranks(ra_unit_space(p.B, p.H, p.Hkv, p.S, p.N, p.layout, p.causal,
+                                                             s_begin, s_end),
+                                               rank_lo, rank_hi);
     const int variant = g_kernel_variant.load(std::memory_order_relaxed);
     a.cluster = variant == 1 ? 1 : 2;
+    if (ra_unit_count(sp) == 0)
+        return ra::launch_attn_tc(a, st) == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+    // Large problems (the order grouped by kv head, from 2^19 key/value rows)
+    // go kv head by kv head, one launch per (batch, kv head) on contiguous
+    // slices: the heads are independent and each alone still fills the GPU,
+    // and dealing each head's heaviest-first units from round 0 balances the
+    // CTAs better than one snake over all heads, whose heavy-to-light runs
+    // fall out of phase with the rounds (host simulation of the dealing at
+    // 256K tokens: 2.3 % of idle tail against 0.1 %; measured +2 % at 256K,
+    // +1 % at 1M tokens).  Every unit is computed as in the single launch.
+    if (nsplit == 1 && sp.kv_outer && (long long)p.B * p.Hkv > 1) {
+        const int g = p.H / p.Hkv;
+        const long long q_head = (long long)g * p.S * p.d, kv_head = (long long)p.S * p.d;
+        const int out_esz = out_f32 ? 4 : 2;
+        for (long long bh = 0; bh < (long long)p.B * p.Hkv; ++bh) {
+            ra::TcLaunch b = a;
+            b.B = 1, b.H = g, b.Hkv = 1;
+            b.q = static_cast<const char *>(q) + bh * q_head * 2;
+            b.k = static_cast<const char *>(k) + bh * kv_head * 2;
+            b.v = static_cast<const char *>(v) + bh * kv_head * 2;
+            b.out = static_cast<char *>(out) + bh * q_head * out_esz;
+            b.lse = lse + bh * g * p.S;
+            count_launch();
+            if (ra::launch_attn_tc(b, st) != cudaSuccess)
+                return RA_ERR_CUDA;
+        }
+        return RA_OK;
+    }
+    count_launch();
     return ra::launch_attn_tc(a, st) == cudaSuccess ? RA_OK : RA_ERR_CUDA;
 }
 
