@@ -34,6 +34,7 @@
 // (dK/dV kernel) or dQ (dQ kernel) from column 256.
 #include <cstdint>
 #include <cstring>
+#include <type_traits>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -642,35 +643,54 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dq_kernel(const __grid_
                 __syncwarp();
             }
         }
-        for (int n = 0; ok && n < T; ++n) {
-            if (!(ok = ww(bar(ctrl->p_full), n & 1, BS_P_FULL)))
-                break;
+        // One key tile per step, specialised on n mod 6 (K in three stages,
+        // V and the S buffers in two), so every address below is a base plus a
+        // constant.
+        static_assert(C::Q_KST == 3, "dQ step specialisation assumes three K stages");
+        auto step = [&](auto ph_c, int n) -> bool {
+            constexpr int PH = decltype(ph_c)::value;
+            constexpr uint32_t KS = PH % 3, KS2 = (PH + 2) % 3, VS1 = (PH + 1) & 1;
+            constexpr uint32_t SBUF = (PH & 1) ? 384u : 0u;
+            if (!ww(bar(ctrl->p_full), n & 1, BS_P_FULL))
+                return false;
             tc_fence_after();
             if (n + 1 < T) {
-                if (!(ok = wait_v(n + 1)))
-                    break;
+                if (!ww(bar(ctrl->st_full[VS1]), ((n + 1) >> 1) & 1, BS_ST_FULL))
+                    return false;
                 tc_fence_after();
                 if (leader) {
-                    issue_rows_dot<D>(tm + 128, sDO, sV(n + 1));  // dP(n+1): dP(n) was read
+                    issue_rows_dot<D>(tm + 128, sDO, sb + C::Q_OFF_V + VS1 * C::TILE);  // dP(n+1): dP(n) was read
                     mma_commit(bar(ctrl->dp_full));
-                    mma_commit(bar(ctrl->st_empty[(n + 1) & 1]));
+                    mma_commit(bar(ctrl->st_empty[VS1]));
                 }
                 __syncwarp();
             }
             if (leader) {
-                issue_tmem_times_tile<D>(tm + 256, tm + ((n & 1) ? 384u : 0u), sK(n), n > 0);  // dQ += dS K
-                mma_commit(bar(ctrl->ke[n % C::Q_KST]));
+                issue_tmem_times_tile<D>(tm + 256, tm + SBUF, sb + C::Q_OFF_K + KS * C::TILE, n > 0);  // dQ += dS K
+                mma_commit(bar(ctrl->ke[KS]));
             }
             __syncwarp();
             if (n + 2 < T) {
-                if (!(ok = wait_k(n + 2)))
-                    break;
+                if (!ww(bar(ctrl->kf[KS2]), ((n + 2) / 3) & 1, BS_ST_FULL))
+                    return false;
                 tc_fence_after();
                 if (leader) {
-                    issue_rows_dot<D>(tm + ((n & 1) ? 384u : 0u), sQ, sK(n + 2));  // dS(n) consumed in order
-                    mma_commit(bar(ctrl->s_full[n & 1]));
+                    issue_rows_dot<D>(tm + SBUF, sQ, sb + C::Q_OFF_K + KS2 * C::TILE);  // dS(n) consumed in order
+                    mma_commit(bar(ctrl->s_full[PH & 1]));
                 }
                 __syncwarp();
+            }
+            return true;
+        };
+        using std::integral_constant;
+        for (int n = 0; ok && n < T; ++n) {
+            switch (n % 6) {
+            case 0: ok = step(integral_constant<int, 0>{}, n); break;
+            case 1: ok = step(integral_constant<int, 1>{}, n); break;
+            case 2: ok = step(integral_constant<int, 2>{}, n); break;
+            case 3: ok = step(integral_constant<int, 3>{}, n); break;
+            case 4: ok = step(integral_constant<int, 4>{}, n); break;
+            default: ok = step(integral_constant<int, 5>{}, n); break;
             }
         }
         if (leader)
