@@ -364,37 +364,45 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dkdv_kernel(const __gri
                 __syncwarp();
             }
         }
-        for (int n = 0; ok && n < T; ++n) {
+        // One query tile per step, specialised on the stage parity (Q and dO
+        // in two stages): every address below is a base plus a constant.
+        auto step = [&](auto st_c, int n) -> bool {
+            constexpr uint32_t ST = decltype(st_c)::value, ST1 = ST ^ 1u;
+            const uint32_t sQn = sb + C::KV_OFF_Q + ST * C::TILE, sDOn = sb + C::KV_OFF_DO + ST * C::TILE;
+            const uint32_t sQ1 = sb + C::KV_OFF_Q + ST1 * C::TILE, sDO1 = sb + C::KV_OFF_DO + ST1 * C::TILE;
             const bool next = n + 1 < T;
-            if (!(ok = ww(bar(ctrl->p_full), n & 1, BS_P_FULL)))
-                break;
+            if (!ww(bar(ctrl->p_full), n & 1, BS_P_FULL))
+                return false;
             tc_fence_after();
             if (leader)
-                issue_tmem_times_tile<D>(tm + 256, tm, sDO(n), n > 0);  // dV += P^T dO
+                issue_tmem_times_tile<D>(tm + 256, tm, sDOn, n > 0);  // dV += P^T dO
             __syncwarp();
             if (next) {
-                if (!(ok = ww(bar(ctrl->st_full[(n + 1) & 1]), ((n + 1) >> 1) & 1, BS_ST_FULL)))
-                    break;
+                if (!ww(bar(ctrl->st_full[ST1]), ((n + 1) >> 1) & 1, BS_ST_FULL))
+                    return false;
                 tc_fence_after();
                 if (leader) {
-                    issue_rows_dot<D>(tm, sK, sQ(n + 1));  // S^T(n+1): P^T(n) consumed in order
+                    issue_rows_dot<D>(tm, sK, sQ1);  // S^T(n+1): P^T(n) consumed in order
                     mma_commit(bar(ctrl->s_full[0]));
                 }
                 __syncwarp();
             }
-            if (!(ok = ww(bar(ctrl->ds_full), n & 1, BS_S_FULL)))
-                break;
+            if (!ww(bar(ctrl->ds_full), n & 1, BS_S_FULL))
+                return false;
             tc_fence_after();
             if (leader) {
-                issue_tmem_times_tile<D>(tm + 256 + D, tm + 128, sQ(n), n > 0);  // dK += dS^T Q
-                mma_commit(bar(ctrl->st_empty[n & 1]));
+                issue_tmem_times_tile<D>(tm + 256 + D, tm + 128, sQn, n > 0);  // dK += dS^T Q
+                mma_commit(bar(ctrl->st_empty[ST]));
                 if (next) {
-                    issue_rows_dot<D>(tm + 128, sV, sDO(n + 1));  // dP^T(n+1): dS^T(n) consumed in order
+                    issue_rows_dot<D>(tm + 128, sV, sDO1);  // dP^T(n+1): dS^T(n) consumed in order
                     mma_commit(bar(ctrl->dp_full));
                 }
             }
             __syncwarp();
-        }
+            return true;
+        };
+        for (int n = 0; ok && n < T; ++n)
+            ok = (n & 1) ? step(std::integral_constant<uint32_t, 1>{}, n) : step(std::integral_constant<uint32_t, 0>{}, n);
         if (leader)
             mma_commit(bar(ctrl->final_bar));
         __syncwarp();
