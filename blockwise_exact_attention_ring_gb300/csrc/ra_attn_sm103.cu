@@ -20,7 +20,8 @@
 //     (two heads of one grouped-query group, or two adjacent tiles of one
 //     head), so every key/value tile staged in shared memory feeds two tiles;
 //   * warp 0 issues TMA loads (Q once per unit, K and V per 128-key tile, in
-//     128-byte swizzled 64-column slabs), warp 1 issues tcgen05.mma,
+//     128-byte swizzled 64-column slabs), warp 1 issues tcgen05.mma (each
+//     a whole warp on warp-uniform values, one elected lane issuing),
 //     warps 4-7 and 8-11 run the online softmax for query tile 0 and 1;
 //   * S = Q K^T goes to TMEM (fp32, 128 lanes x 128 columns per tile); each
 //     softmax thread reads its row once (two 64-column loads, one wait; the

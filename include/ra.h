@@ -84,7 +84,9 @@ typedef enum {
 typedef enum { RA_LAYOUT_CONTIGUOUS = 0, RA_LAYOUT_STRIPED = 1 } ra_layout;
 
 /* RA_MODE_FUSED: one persistent launch walks, for every query tile, the key
- *   blocks in ring order and keeps the running softmax on chip.
+ *   blocks in ring order and keeps the running softmax on chip (problems of
+ *   2^19 key/value rows and more: one such launch per (batch, kv head), the
+ *   heads being independent; the results are those of a single launch).
  * RA_MODE_PER_STEP: one launch per ring step s writes that step's partial
  *   (out_s, lse_s) for every rank, then ra_merge-style merging folds it into
  *   the running result, as each ring device would after receiving a block.

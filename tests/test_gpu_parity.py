@@ -271,3 +271,28 @@ def test_bf16_d64_long_walks(layout, spikes):
     ra.check()
     rows = inputs.sample_rows(B, H, S, N, n=1024, seed=11).numpy()
     _check(out, lse, q, k, v, True, rows=rows)
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+def test_per_kv_head_launches_with_batch(layout):
+    """From 2^19 key/value rows the library launches the kernel once per
+    (batch, kv head) on slices of q, k, v, out and lse.  B = 2 and four kv
+    heads (2 x 4 x 65536 = 2^19 rows) take that path with slices that start
+    in the second batch entry: sampled rows against the oracle, and the whole
+    output bit for bit against the same problem computed head by head below
+    the threshold (one kv head per call: B = 1, Hkv = 1, a single launch)."""
+    B, H, Hkv, S, d, N = 2, 8, 4, 65536, 64, 8
+    assert B * Hkv * S >= 1 << 19
+    q, k, v = _dev(*inputs.make_qkv(B, H, Hkv, S, d, seed=77))
+    out, lse = ra.forward(q, k, v, n_blocks=N, layout=layout, causal=True)
+    ra.check()
+    rows = inputs.sample_rows(B, H, S, N, n=512, seed=13).numpy()
+    _check(out, lse, q, k, v, True, rows=rows)
+    g = H // Hkv
+    for b in range(B):
+        for h in range(Hkv):
+            o1, l1 = ra.forward(q[b:b + 1, h * g:(h + 1) * g].contiguous(), k[b:b + 1, h:h + 1].contiguous(),
+                                v[b:b + 1, h:h + 1].contiguous(), n_blocks=N, layout=layout, causal=True)
+            assert torch.equal(o1, out[b:b + 1, h * g:(h + 1) * g])
+            assert torch.equal(l1, lse[b:b + 1, h * g:(h + 1) * g])
+    ra.check()
