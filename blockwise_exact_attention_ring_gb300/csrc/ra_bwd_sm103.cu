@@ -634,10 +634,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dq_kernel(const __grid_
             if (!(ok = wait_k(n)))
                 break;
             tc_fence_after();
-            if (leader) {
-                issue_rows_dot<D>(tm + (n ? 384u : 0u), sQ, sK(n));
-                mma_commit(bar(ctrl->s_full[n]));
-            }
+            if (leader)
+                issue_rows_dot<D>(tm + (n ? 384u : 0u), sQ, sK(n));  // S(n): tracked by dP(n)'s commit
             __syncwarp();
             if (n == 0) {
                 if (!(ok = wait_v(0)))
@@ -682,10 +680,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dq_kernel(const __grid_
                 if (!ww(bar(ctrl->kf[KS2]), ((n + 2) / 3) & 1, BS_ST_FULL))
                     return false;
                 tc_fence_after();
-                if (leader) {
-                    issue_rows_dot<D>(tm + SBUF, sQ, sb + C::Q_OFF_K + KS2 * C::TILE);  // dS(n) consumed in order
-                    mma_commit(bar(ctrl->s_full[PH & 1]));
-                }
+                if (leader)  // dS(n) consumed in order; S(n + 2) is tracked by dP(n + 2)'s commit
+                    issue_rows_dot<D>(tm + SBUF, sQ, sb + C::Q_OFF_K + KS2 * C::TILE);
                 __syncwarp();
             }
             return true;
@@ -727,8 +723,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ra_bwd_dq_kernel(const __grid_
         w.start(i, ta, p.N, p.layout, p.causal, p.ntiles);
         for (; w.valid(); w.advance(), ++n) {
             const uint32_t tS = tmem + lane_off + ((n & 1) ? 384u : 0u);
-            if (!(ok = bwait_warp(p.status, bar(ctrl->s_full[n & 1]), (n >> 1) & 1, abort, tmo, BS_S_FULL)))
-                break;
+            // S(n) was issued before dP(n) by the same thread, and the commit
+            // that signals dP(n) tracks every earlier MMA: one wait covers both
             if (!(ok = bwait_warp(p.status, bar(ctrl->dp_full), n & 1, abort, tmo, BS_S_FULL)))
                 break;
             tc_fence_after();
