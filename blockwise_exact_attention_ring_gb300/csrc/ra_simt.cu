@@ -622,6 +622,10 @@ __global__ void ra_combine_kernel(const float *__restrict__ part, const float *_
                                   FastDiv fS, FastDiv fL)
 {
     const int vpr = d / 4;  // 16-byte vectors per row
+    // launched as a programmatic dependent of the attention kernel: the CTAs
+    // may start while its last CTAs finish, and wait here until its writes
+    // (the partials) are complete and visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (NARROW) {
         const uint32_t n = (uint32_t)(rows_total * vpr);
         for (uint32_t idx = blockIdx.x * blockDim.x + threadIdx.x; idx < n; idx += gridDim.x * blockDim.x) {
@@ -665,22 +669,31 @@ void launch_combine(const float *part, const float *part_lse, int nsplit, long l
     const int L = S / N;
     const bool narrow = rows_total * (d / 4) < (1ll << 31);
     const FastDiv fv = make_fastdiv((uint32_t)(d / 4)), fS = make_fastdiv((uint32_t)S), fL = make_fastdiv((uint32_t)L);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(threads);
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
     if (out_bf16) {
         auto *o = (__nv_bfloat16 *)out;
         if (narrow)
-            ra_combine_kernel<__nv_bfloat16, true><<<(int)blocks, threads, 0, st>>>(
-                part, part_lse, nsplit, part_stride, o, lse, rows_total, S, L, N, striped, d, fv, fS, fL);
+            cudaLaunchKernelEx(&cfg, ra_combine_kernel<__nv_bfloat16, true>, part, part_lse, nsplit, part_stride, o,
+                               lse, rows_total, S, L, N, striped, d, fv, fS, fL);
         else
-            ra_combine_kernel<__nv_bfloat16, false><<<(int)blocks, threads, 0, st>>>(
-                part, part_lse, nsplit, part_stride, o, lse, rows_total, S, L, N, striped, d, fv, fS, fL);
+            cudaLaunchKernelEx(&cfg, ra_combine_kernel<__nv_bfloat16, false>, part, part_lse, nsplit, part_stride, o,
+                               lse, rows_total, S, L, N, striped, d, fv, fS, fL);
     } else {
         auto *o = (float *)out;
         if (narrow)
-            ra_combine_kernel<float, true><<<(int)blocks, threads, 0, st>>>(
-                part, part_lse, nsplit, part_stride, o, lse, rows_total, S, L, N, striped, d, fv, fS, fL);
+            cudaLaunchKernelEx(&cfg, ra_combine_kernel<float, true>, part, part_lse, nsplit, part_stride, o, lse,
+                               rows_total, S, L, N, striped, d, fv, fS, fL);
         else
-            ra_combine_kernel<float, false><<<(int)blocks, threads, 0, st>>>(
-                part, part_lse, nsplit, part_stride, o, lse, rows_total, S, L, N, striped, d, fv, fS, fL);
+            cudaLaunchKernelEx(&cfg, ra_combine_kernel<float, false>, part, part_lse, nsplit, part_stride, o, lse,
+                               rows_total, S, L, N, striped, d, fv, fS, fL);
     }
 }
 
