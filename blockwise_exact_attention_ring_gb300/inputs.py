@@ -74,6 +74,12 @@ WORKLOADS: Dict[str, Workload] = {w.name: w for w in [
              LAYOUT_STRIPED, True, "bf16", 1006),
     Workload("ring8-s128k-h32kv8-d128-causal-striped", 1, 32, 8, 131072, 128, 8,
              LAYOUT_STRIPED, True, "bf16", 1007),
+    # one kv head of the 256K striped workload (its four query heads): the
+    # 256K workload runs one launch per kv head, each exactly this problem,
+    # so one capture of this launch times eight is a 256K step (~1.5 GB on
+    # the device)
+    Workload("ring8-s256k-h4kv1-d128-causal-striped", 1, 4, 1, 262144, 128, 8,
+             LAYOUT_STRIPED, True, "bf16", 1008),
 ]}
 
 
