@@ -22,7 +22,10 @@
 //   * warp 0 issues TMA loads (Q once per unit, K and V per 128-key tile, in
 //     128-byte swizzled 64-column slabs), warp 1 issues tcgen05.mma (each
 //     a whole warp on warp-uniform values, one elected lane issuing),
-//     warps 4-7 and 8-11 run the online softmax for query tile 0 and 1;
+//     warps 4-7 and 8-11 run the online softmax for query tile 0 and 1 (at
+//     d = 64, warps 4-11 and 12-19, two threads per row, one per 64-key
+//     half of each key tile, each half with its own running max, sum and O,
+//     merged in the epilogue);
 //   * S = Q K^T goes to TMEM (fp32, 128 lanes x 128 columns per tile); each
 //     softmax thread reads its row once (two 64-column loads, one wait; the
 //     loads of an unmasked tile also reduce the row to its max, a Blackwell
@@ -37,7 +40,8 @@
 //     frees TMEM and returns.
 //
 // TMEM columns: S/P tile 0 [0,128), S/P tile 1 [128,256), O tile 0
-// [256,256+d), O tile 1 [384,384+d).
+// [256,256+d), O tile 1 [384,384+d); at d = 64 the two halves' O of tile t
+// are [256+128t, 320+128t) and [320+128t, 384+128t).
 #include <atomic>
 #include <cstdint>
 #include <mutex>
@@ -57,7 +61,6 @@ __device__ unsigned int g_ra_status = 0;
 
 namespace {
 
-constexpr int NUM_THREADS = 384;  // 12 warps: TMA, MMA, 2 spare, 2 x 4 softmax
 constexpr uint32_t TMEM_COLS = 512;
 
 enum Site : unsigned int {
@@ -67,6 +70,12 @@ enum Site : unsigned int {
 
 template <int D>
 struct Cfg {
+    // softmax threads per query row: at d = 128 one thread takes the row's 128
+    // key columns; at d = 64 (where a tile's MMAs are half as long and cover
+    // half as much of the softmax) two threads take 64 columns each, with
+    // their own running max, sum and O (TMEM: 2 tiles x (128 S + 2 x 64 O))
+    static constexpr int HALVES = D == 64 ? 2 : 1;
+    static constexpr int THREADS = 128 + 2 * 128 * HALVES;  // TMA, MMA, 2 spare warps, softmax
     static constexpr int KSTAGES = 2;
     static constexpr int VSTAGES = 2;
     static constexpr int SLAB = 128 * 64 * 2;  // 128 rows x 64 bf16 (128 B swizzled rows)
@@ -76,13 +85,16 @@ struct Cfg {
     static constexpr int OFF_K = OFF_Q + 2 * TILE;
     static constexpr int OFF_V = OFF_K + KSTAGES * TILE;
     static constexpr int OFF_CTRL = OFF_V + VSTAGES * TILE;
-    static constexpr int SMEM = OFF_CTRL + 256 + 1024;  // control block + alignment slack
+    static constexpr int OFF_XCH = OFF_CTRL + 256;  // (m, l) of each row's halves: [unit parity][tile][half][row]
+    static constexpr int XCH = HALVES == 2 ? 2 * 2 * 2 * 128 * 8 : 0;
+    static constexpr int SMEM = OFF_XCH + XCH + 1024;  // + alignment slack
 };
 
 struct Ctrl {
     uint64_t q_full, q_empty;
     uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
     uint64_t s_full[2], p_full[2], o_done[2], o_free[2];  // o_done: once per unit, after its last P V
+    uint64_t x_full[2];  // both halves of a tile's rows have posted (m, l)
     uint64_t final_bar;
     uint32_t tmem_base;
     int abort;
@@ -182,7 +194,7 @@ __device__ __forceinline__ void load_tile_both(uint32_t dst, const CUtensorMap *
 // TMA multicast, and a stage is reloaded only after both CTAs' MMAs have
 // consumed it (each MMA warp commits to the empty barrier of both CTAs).
 template <int D, int CL, bool SPLIT>
-__global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid_constant__ TcParams p)
+__global__ void __launch_bounds__(Cfg<D>::THREADS, 1) ra_attn_tc_kernel(const __grid_constant__ TcParams p)
 {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -208,9 +220,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(ctrl->s_full[t]), 1);
-            mbar_init(bar(ctrl->p_full[t]), 128);
+            mbar_init(bar(ctrl->p_full[t]), 128 * C::HALVES);
             mbar_init(bar(ctrl->o_done[t]), 1);
-            mbar_init(bar(ctrl->o_free[t]), 128);
+            mbar_init(bar(ctrl->o_free[t]), 128 * C::HALVES);
+            if (C::HALVES == 2)
+                mbar_init(bar(ctrl->x_full[t]), 128 * C::HALVES);
         }
         mbar_init(bar(ctrl->final_bar), 1);
         ctrl->abort = 0;
@@ -355,9 +369,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
         auto issue_pv = [&](int t, int vs, bool acc) {
             const uint32_t va = sV + vs * C::TILE;
 #pragma unroll
-            for (int kk = 0; kk < RA_TILE / 16; ++kk)
-                mma_ts(tm + 256 + t * 128, tm + t * 128 + kk * 8, smem_desc_sw128(va + kk * 2048, C::SLAB, 1024),
-                       IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < RA_TILE / 16; ++kk) {
+                if constexpr (C::HALVES == 2) {
+                    // keys [0, 64) and [64, 128) go to the two halves' own O,
+                    // each reading P from the first 32 columns of its half
+                    const int hh = kk >> 2;
+                    mma_ts(tm + 256 + t * 128 + hh * D, tm + t * 128 + hh * 64 + (kk & 3) * 8,
+                           smem_desc_sw128(va + kk * 2048, C::SLAB, 1024), IDESC_PV, (acc || (kk & 3) > 0) ? 1u : 0u);
+                } else {
+                    mma_ts(tm + 256 + t * 128, tm + t * 128 + kk * 8, smem_desc_sw128(va + kk * 2048, C::SLAB, 1024),
+                           IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+                }
+            }
         };
         auto wwait = [&](uint32_t b, uint32_t parity, unsigned int site) {
             return wait_warp(b, parity, abort, tmo, site);
@@ -464,7 +487,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
         wait_drain(bar(ctrl->final_bar), 0, tmo);
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax
-        const int t = (warp - 4) >> 2;
+        // warps 4 + 4 HALVES t + 4 h + qw: tile t, column half h, rows 32 qw..
+        const int t = (warp - 4) >> (C::HALVES == 2 ? 3 : 2);
+        const int h = C::HALVES == 2 ? ((warp - 4) >> 2) & 1 : 0;
         const int qw = warp & 3;
         const int r = qw * 32 + lane;
         const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
@@ -485,7 +510,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
             const int a = ta * RA_TILE + r;
             if (SPLIT && cnt == 0) {
                 // an empty piece: its partial holds no key (lse = -inf)
-                if (store && a < p.L)
+                if (store && a < p.L && h == 0)
                     p.lse[k * p.split_lse_stride + (long long)bh * p.S + (long long)U.rank * p.L + a] = -INFINITY;
                 continue;
             }
@@ -506,11 +531,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
                 const int lim = ra_key_limit(w.cls, a, p.L) - w.tb * RA_TILE;
                 // masked only where some column of the warp's rows lies past
                 // its visibility bound (diagonal and ragged tiles)
-                const bool masked = !__all_sync(0xffffffffu, lim >= RA_TILE);
-                if (masked)
-                    softmax_step<D, true>(tS, tO, lim, sl2, jj > 0, m_run, l_run);
-                else
-                    softmax_step<D, false>(tS, tO, lim, sl2, jj > 0, m_run, l_run);
+                if constexpr (C::HALVES == 2) {
+                    const int limh = lim - 64 * h;
+                    if (!__all_sync(0xffffffffu, limh >= 64))
+                        softmax_half<D, true>(tS + 64 * h, tO + D * h, limh, sl2, jj > 0, m_run, l_run);
+                    else
+                        softmax_half<D, false>(tS + 64 * h, tO + D * h, limh, sl2, jj > 0, m_run, l_run);
+                } else {
+                    const bool masked = !__all_sync(0xffffffffu, lim >= RA_TILE);
+                    if (masked)
+                        softmax_step<D, true>(tS, tO, lim, sl2, jj > 0, m_run, l_run);
+                    else
+                        softmax_step<D, false>(tS, tO, lim, sl2, jj > 0, m_run, l_run);
+                }
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(bar(ctrl->p_full[t]));
@@ -524,11 +557,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ra_attn_tc_kernel(const __grid
             tc_fence_after();
             const bool valid = store && a < p.L;
             const long long orow = (long long)bh * p.S + (long long)U.rank * p.L + a;
-            if (SPLIT)
-                store_row<D>(tO, valid, orow, m_run, l_run, static_cast<char *>(p.out) + k * p.split_out_bytes,
-                             p.lse + k * p.split_lse_stride, 1);
-            else
-                store_row<D>(tO, valid, orow, m_run, l_run, p.out, p.lse, p.out_f32);
+            if constexpr (C::HALVES == 2) {
+                // post this half's (m, l), wait (bounded) for the other half's
+                const uint32_t par = (ocnt - 1) & 1;
+                float2 *xch = reinterpret_cast<float2 *>(smem + C::OFF_XCH) + (par * 2 + t) * 256;
+                xch[h * 128 + r] = make_float2(m_run, l_run);
+                mbar_arrive(bar(ctrl->x_full[t]));
+                if (!(ok = wait_warp(bar(ctrl->x_full[t]), par, abort, tmo, SITE_O_DONE)))
+                    break;
+                const float2 oth = xch[(h ^ 1) * 128 + r];
+                if (SPLIT)
+                    merge_halves_store_row<D>(tO, h, valid, orow, m_run, l_run, oth.x, oth.y,
+                                              static_cast<char *>(p.out) + k * p.split_out_bytes,
+                                              p.lse + k * p.split_lse_stride, 1);
+                else
+                    merge_halves_store_row<D>(tO, h, valid, orow, m_run, l_run, oth.x, oth.y, p.out, p.lse,
+                                              p.out_f32);
+            } else {
+                if (SPLIT)
+                    store_row<D>(tO, valid, orow, m_run, l_run, static_cast<char *>(p.out) + k * p.split_out_bytes,
+                                 p.lse + k * p.split_lse_stride, 1);
+                else
+                    store_row<D>(tO, valid, orow, m_run, l_run, p.out, p.lse, p.out_f32);
+            }
             __syncwarp();
             tc_fence_before();
             mbar_arrive(bar(ctrl->o_free[t]));
@@ -600,7 +651,7 @@ int max_pair_clusters()
         return have - 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2);
-    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.blockDim = dim3(Cfg<D>::THREADS);
     cfg.dynamicSmemBytes = Cfg<D>::SMEM;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -633,7 +684,7 @@ cudaError_t launch_grid(const TcParams &p, bool clusters, int sm_count, cudaStre
             const int n_cl = pairs < max_cl ? pairs : max_cl;
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2 * n_cl);
-            cfg.blockDim = dim3(NUM_THREADS);
+            cfg.blockDim = dim3(C::THREADS);
             cfg.dynamicSmemBytes = C::SMEM;
             cfg.stream = st;
             cudaLaunchAttribute at[1];
@@ -650,7 +701,7 @@ cudaError_t launch_grid(const TcParams &p, bool clusters, int sm_count, cudaStre
     if ((e = set_smem_attr<D, 1, SPLIT>()) != cudaSuccess)
         return e;
     const int grid = p.n_items < sm_count ? p.n_items : sm_count;
-    ra_attn_tc_kernel<D, 1, SPLIT><<<grid, NUM_THREADS, C::SMEM, st>>>(p);
+    ra_attn_tc_kernel<D, 1, SPLIT><<<grid, C::THREADS, C::SMEM, st>>>(p);
     return cudaGetLastError();
 }
 
