@@ -282,18 +282,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn_maj
          | ((uint32_t)(M >> 4) << 24);       // M / 16
 }
 
-// Register budget hand-off between warpgroups (all warps of a warpgroup).
-template <int N>
-__device__ __forceinline__ void regs_dec()
-{
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N>
-__device__ __forceinline__ void regs_inc()
-{
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 __device__ __forceinline__ float ex2_approx(float x)
 {
     float y;
