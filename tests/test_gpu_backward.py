@@ -102,14 +102,21 @@ KEY_ROWS = {
                    (5, S - 1), (5, S - 2), (5, S - 128), (5, S - 1000)],
     "ring8-s256k-h32kv8-d128-causal-striped":
         lambda S: [(g, S - o) for g in (0, 7) for o in (1, 2, 8, 9, 100, 257, 511, 512)],
+    # the other lines whose backward the bench measures: late keys only (an
+    # early key's oracle would recompute hundreds of thousands of softmax rows)
+    "ring8-s256k-h32kv8-d128-causal-contiguous":
+        lambda S: [(g, S - o) for g in (0, 7) for o in (1, 2, 8, 9, 100, 257, 511, 512)],
+    "ring32-s1m-h32kv8-d128-causal-striped":
+        lambda S: [(g, S - o) for g in (0, 7) for o in (1, 2, 33, 100, 257, 512)],
 }
 
 
 @pytest.mark.parametrize("name", list(KEY_ROWS))
 def test_backward_workload_sampled_rows(name):
     """A workload's full shape, in its own layout (32K tokens over 4
-    contiguous blocks; 256K tokens over 8, striped, as the bench's backward
-    measurement runs): dq on sampled query rows and dk, dv on sampled key rows
+    contiguous blocks; 256K tokens over 8, striped and contiguous; 1M tokens
+    over 32, striped: every line whose backward the bench measures): dq on
+    sampled query rows and dk, dv on sampled key rows
     against the fp64 oracle row by row, each at the per-tensor bar
     2e-2 * max |ref| over the compared rows; and over all keys the identities
     sum_u dV = sum_t dO (per kv head) and sum_u dK = 0, which the whole dK
@@ -122,23 +129,28 @@ def test_backward_workload_sampled_rows(name):
     out, lse = ra.forward(q, k, v, n_blocks=w.n_blocks, layout=layout, causal=True)
     dq, dk, dv = ra.backward(q, k, v, out, lse, dout, w.n_blocks, layout=layout, causal=True)
     ra.check()
+    def picked(x, rows):  # the selected rows only, gathered on the device
+        idx = torch.as_tensor(np.asarray(rows), device=x.device)
+        return x.reshape(-1, w.d)[idx].double().cpu().numpy()
+
     qc, kc, vc, dc = (t.cpu() for t in (q, k, v, dout))
     rows = inputs.sample_rows(w.B, w.H, w.S, w.n_blocks, n=48 if w.S > 65536 else 96, seed=7)
     ref = dq_rows(qc, kc, vc, dc, rows, causal=True)
-    got = dq.float().cpu().double().numpy().reshape(-1, w.d)[rows]
+    got = picked(dq, rows)
     assert np.abs(got - ref).max() <= REL_MAX * np.abs(ref).max()
     key_rows = np.array([gg * w.S + u for gg, u in KEY_ROWS[name](w.S)])  # B = 1
     ref_k, ref_v = dkdv_rows(qc, kc, vc, dc, key_rows, causal=True)
-    got_k = dk.float().cpu().double().numpy().reshape(-1, w.d)[key_rows]
-    got_v = dv.float().cpu().double().numpy().reshape(-1, w.d)[key_rows]
+    got_k, got_v = picked(dk, key_rows), picked(dv, key_rows)
     assert np.abs(got_k - ref_k).max() <= REL_MAX * np.abs(ref_k).max()
     assert np.abs(got_v - ref_v).max() <= REL_MAX * np.abs(ref_v).max()
+    del qc, kc, vc, dc
     grp = w.H // w.Hkv
-    dv_sum = dv.double().sum(dim=2)
-    do_sum = dout.double().reshape(w.B, w.Hkv, grp, w.S, w.d).sum(dim=(2, 3))
-    assert (dv_sum - do_sum).abs().max().item() <= 1e-2 * dout.double().abs().sum(dim=2).max().item()
-    dk_sum = dk.double().sum(dim=2)
-    assert dk_sum.abs().max().item() <= 1e-2 * dk.double().abs().sum(dim=2).max().item()
+    f64 = torch.float64
+    dv_sum = dv.sum(dim=2, dtype=f64)
+    do_sum = dout.reshape(w.B, w.Hkv, grp, w.S, w.d).sum(dim=(2, 3), dtype=f64)
+    assert (dv_sum - do_sum).abs().max().item() <= 1e-2 * dout.abs().sum(dim=2, dtype=f64).max().item()
+    dk_sum = dk.sum(dim=2, dtype=f64)
+    assert dk_sum.abs().max().item() <= 1e-2 * dk.abs().sum(dim=2, dtype=f64).max().item()
 
 
 F32_CASES = [
