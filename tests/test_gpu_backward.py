@@ -44,6 +44,7 @@ CASES = [
     (1, 2, 1, 600, 128, 3, "striped", True),      # L = 200: ragged tiles
     (1, 4, 4, 384, 128, 3, "contiguous", False),
     (1, 6, 2, 768, 64, 2, "striped", False),
+    (1, 4, 4, 4096, 64, 2, "contiguous", False),  # the pages' context-parallel example shape
 ]
 
 
